@@ -1,0 +1,307 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by mathematics.
+
+Each test ties one oracle step to something other than the oracle itself: a
+hand-worked example, a closed form printed on the pages, a brute-force enumeration,
+a library routine, a Monte Carlo estimate of a probability the pages state, or an
+invariant. Sources: "MagicPIG: LSH Sampling for Efficient LLM Generation"
+(arXiv 2410.16179v2) and the authors' responses to reviews (paperhub page).
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+from scipy import stats
+from scipy.special import softmax
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------------
+# hand-worked example (tests/golden)
+# ----------------------------------------------------------------------------------
+
+def test_golden_tiny_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "tiny_2d_worked_example.json")))
+    keys = np.array(g["keys"], float)
+    vals = np.array(g["values"], float)
+    W = np.array(g["W"], float)
+    q = np.array(g["q"], float)
+    K, L, s, w, n0 = g["K"], g["L"], g["n_sink"], g["window"], g["n_prefill"]
+    ex = g["expected"]
+    tables = O.HeadTables(keys, W, K, L, s, n0)
+    np.testing.assert_allclose(tables.center, ex["center"], atol=1e-15)
+    np.testing.assert_array_equal(tables.codes, ex["key_codes"])
+    r = O.decode_head(q, keys, vals, tables, n0, w)
+    np.testing.assert_array_equal(r["q_code"], ex["q_code"])
+    np.testing.assert_array_equal(r["S"], ex["S"])
+    np.testing.assert_array_equal(r["T"], ex["T"])
+    # arccos is ill-conditioned at cos = 1: a rounding of cos by 1 ulp moves p by ~1e-8
+    np.testing.assert_allclose(r["p"], [float(Fraction(x)) for x in ex["p"]], atol=1e-7)
+    np.testing.assert_allclose(r["u"], [float(Fraction(x)) for x in ex["u"]], rtol=1e-12)
+    env = {"exp": math.exp, "sqrt": math.sqrt}
+    wts = {int(i): eval(e, env) for i, e in ex["weights"].items()}
+    tot = sum(wts.values())
+    want = np.array([sum(wt * vals[i][0] for i, wt in wts.items()) / tot, 1.0])
+    np.testing.assert_allclose(r["out"], want, rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------------
+# a1 centering
+# ----------------------------------------------------------------------------------
+
+def test_center_is_known_mean_of_non_sink_prefill():
+    rng = np.random.default_rng(5)
+    d, s, n0 = 6, 4, 40
+    a = rng.normal(size=d)
+    half = rng.normal(size=((n0 - s) // 2, d))
+    z = np.concatenate([half, -half])            # sums to zero over [s, n0)
+    keys = np.concatenate([1e6 * rng.normal(size=(s, d)),   # sinks: must not enter the mean
+                           a + z,
+                           1e6 * rng.normal(size=(5, d))])  # appended later: must not enter
+    np.testing.assert_allclose(O.center_of_keys(keys, s, n0), a, atol=1e-9)
+
+
+# ----------------------------------------------------------------------------------
+# a2 / a5 SimHash codes
+# ----------------------------------------------------------------------------------
+
+def test_codes_one_hot_projections_by_hand():
+    # columns: e0, e1 | e2, e3 | -e0, e2  (K = 2, L = 3)
+    W = np.zeros((4, 6))
+    W[0, 0] = W[1, 1] = W[2, 2] = W[3, 3] = W[2, 5] = 1.0
+    W[0, 4] = -1.0
+    x = np.array([[1.0, -2.0, 3.0, -4.0],     # y = 1,-2 | 3,-4 | -1, 3
+                  [-1.0, 2.0, -3.0, 4.0]])    # y = -1,2 | -3,4 | 1, -3
+    codes = O.simhash_codes(x, W, K=2, L=3)
+    # bit b of table t is column t*K + b
+    np.testing.assert_array_equal(codes, [[0b01, 0b01, 0b10], [0b10, 0b10, 0b01]])
+
+
+def test_codes_negation_is_complement_and_scale_invariant():
+    rng = np.random.default_rng(1)
+    d, K, L = 16, 5, 9
+    W = rng.normal(size=(d, K * L))
+    x = rng.normal(size=(50, d))
+    c = rng.normal(size=d)
+    codes = O.simhash_codes(x, W, K, L, center=c)
+    mirrored = 2 * c - x                          # x - c  ->  -(x - c)
+    np.testing.assert_array_equal(O.simhash_codes(mirrored, W, K, L, center=c),
+                                  (2 ** K - 1) ^ codes)
+    scaled = c + 7.5 * (x - c)
+    np.testing.assert_array_equal(O.simhash_codes(scaled, W, K, L, center=c), codes)
+
+
+@pytest.mark.parametrize("theta_deg,K", [(30, 3), (75, 2), (120, 1)])
+def test_per_table_collision_rate_monte_carlo(theta_deg, K):
+    """P[code_t(x) = code_t(y)] = (1 - theta/pi)^K over Gaussian hyperplanes
+    (MagicPIG §2.2 SimHash). Each of L = 40000 tables is an independent draw."""
+    rng = np.random.default_rng(theta_deg)
+    d, L = 12, 40000
+    th = math.radians(theta_deg)
+    e0, e1 = np.eye(d)[0], np.eye(d)[1]
+    x = np.array([e0, math.cos(th) * e0 + math.sin(th) * e1])
+    W = rng.normal(size=(d, K * L))
+    codes = O.simhash_codes(x, W, K, L)
+    rate = np.mean(codes[0] == codes[1])
+    want = (1 - th / math.pi) ** K
+    sigma = math.sqrt(want * (1 - want) / L)
+    assert abs(rate - want) < 4 * sigma, (rate, want, sigma)
+
+
+def test_near_tie_mask_flags_small_projections():
+    W = np.array([[1.0, 1.0], [0.0, 1e-7]])
+    x = np.array([[1.0, -1.0]])     # y = 1, 1 - 1e-7
+    x2 = np.array([[1e-7, 1.0]])    # y = 1e-7, ~1e-7: both tiny relative to |x||w|
+    assert not O.near_ties(x, W).any()
+    assert O.near_ties(x2, W).all()
+
+
+# ----------------------------------------------------------------------------------
+# a7 collision / inclusion probability
+# ----------------------------------------------------------------------------------
+
+def test_collision_probability_special_angles():
+    q = np.array([2.0, 1.0])
+    kc = np.array([[4.0, 2.0], [-2.0, -1.0], [-1.0, 2.0], [1.0, 3.0], [0.0, 0.0]])
+    # arccos is ill-conditioned at cos = +-1 (1 ulp of cos moves p by ~1e-8)
+    np.testing.assert_allclose(O.collision_probability(q, kc), [1.0, 0.0, 0.5, 0.75, 0.5],
+                               atol=1e-7)
+
+
+@pytest.mark.parametrize("L,T", [(3, 2), (6, 2), (10, 2), (10, 1), (8, 3)])
+def test_inclusion_probability_enumerates_table_patterns(L, T):
+    """Brute force: sum over all 2^L patterns of per-table collisions (each table
+    collides independently with x = p^K) with at least T collisions."""
+    K = 2
+    for p in [0.05, 0.3, 0.5, 0.71, 0.93, 1.0]:
+        x = p ** K
+        want = 0.0
+        for pat in itertools.product([0, 1], repeat=L):
+            h = sum(pat)
+            if h >= T:
+                want += x ** h * (1 - x) ** (L - h)
+        got = O.inclusion_probability(np.array([p]), K, L, threshold=T)[0]
+        assert got == pytest.approx(want, rel=1e-12, abs=1e-300)
+
+
+def test_inclusion_probability_matches_binomial_tail_and_eq10():
+    K, L = 10, 150
+    p = np.linspace(0.02, 1.0, 200)
+    u = O.inclusion_probability(p, K, L)
+    x = p ** K
+    np.testing.assert_allclose(u, stats.binom.sf(1, L, x), rtol=1e-9)
+    # the printed closed form (Eq. 10) where it does not cancel
+    big = L * x >= 1.0
+    eq10 = 1 - (1 - x) ** L - L * x * (1 - x) ** (L - 1)
+    np.testing.assert_allclose(u[big], eq10[big], rtol=1e-12)
+    # T = 1 is the classic LSH retrieval probability 1 - (1 - p^K)^L (MagicPIG §2.2)
+    u1 = O.inclusion_probability(p, K, L, threshold=1)
+    np.testing.assert_allclose(u1, -np.expm1(L * np.log1p(-np.minimum(x, 1 - 1e-16))), rtol=1e-9)
+    assert np.all(np.diff(u) >= 0)
+
+
+def test_expected_budget_is_the_binomial_tail_at_half():
+    # closed form of the author responses (0.5^K per table) is P[Bin(L, 0.5^K) >= 2]
+    for K, L in [(8, 75), (9, 120), (10, 150)]:
+        x = 0.5 ** K
+        assert O.expected_budget(K, L) == pytest.approx(stats.binom.sf(1, L, x), rel=1e-12)
+
+
+# ----------------------------------------------------------------------------------
+# a6 sampled set: region and statistics
+# ----------------------------------------------------------------------------------
+
+def test_region_and_static_tokens():
+    assert O.lsh_region(10, 2, 3) == (2, 7)
+    np.testing.assert_array_equal(O.exact_tokens(10, 2, 3), [0, 1, 7, 8, 9])
+    np.testing.assert_array_equal(O.sampled_set(np.full(10, 5), 10, 2, 3), [2, 3, 4, 5, 6])
+    assert O.lsh_region(3, 4, 2) == (3, 3)
+    np.testing.assert_array_equal(O.exact_tokens(3, 4, 2), [0, 1, 2])
+    assert O.lsh_region(6, 4, 2) == (4, 4)
+    np.testing.assert_array_equal(O.exact_tokens(6, 4, 2), [0, 1, 2, 3, 4, 5])
+
+
+def test_budget_at_half_collision_probability_equals_closed_form():
+    """Keys whose centered vectors are orthogonal to q have p = 1/2 exactly; the
+    expected sampled fraction is then the pages' closed form
+    1 - (1-0.5^K)^L - L 0.5^K (1-0.5^K)^(L-1)."""
+    rng = np.random.default_rng(11)
+    d, n, K, L, s, w = 12, 400, 3, 8, 4, 8
+    q = np.eye(d)[0] * 1.7
+    keys = np.concatenate([np.zeros((n, 1)), rng.normal(size=(n, d - 1))], axis=1)
+    fr = []
+    for _ in range(300):
+        W = rng.normal(size=(d, K * L))
+        t = O.HeadTables(keys, W, K, L, s, n)
+        r = O.decode_head(q, keys, keys, t, n, w)
+        fr.append(len(r["S"]) / (n - s - w))
+        np.testing.assert_allclose(r["p"], 0.5, atol=1e-12)
+    fr = np.array(fr)
+    want = O.expected_budget(K, L)
+    assert abs(fr.mean() - want) < 4 * fr.std(ddof=1) / math.sqrt(len(fr)), (fr.mean(), want)
+
+
+def _cone(rng, d, n):
+    mu = rng.normal(size=d)
+    mu /= np.linalg.norm(mu)
+    keys = 3 * mu + rng.normal(size=(n, d))
+    keys[0] = -6 * mu
+    q = -2 * mu + rng.normal(size=d)
+    return keys, q
+
+
+def test_expected_sample_size_equals_sum_of_inclusion_probabilities():
+    """E_W |S| = sum_i u_i: u is the true inclusion probability of the sampling rule."""
+    rng = np.random.default_rng(3)
+    d, n, K, L, s, w = 10, 300, 3, 10, 4, 16
+    keys, q = _cone(rng, d, n)
+    sizes, usum = [], None
+    for _ in range(400):
+        W = rng.normal(size=(d, K * L))
+        t = O.HeadTables(keys, W, K, L, s, n)
+        r = O.decode_head(q, keys, keys, t, n, w)
+        sizes.append(len(r["S"]))
+        if usum is None:
+            lo, hi = O.lsh_region(n, s, w)
+            p = O.collision_probability(q, keys[lo:hi] - t.center)
+            usum = O.inclusion_probability(p, K, L).sum()
+    sizes = np.array(sizes, float)
+    assert abs(sizes.mean() - usum) < 4 * sizes.std(ddof=1) / math.sqrt(len(sizes)), (sizes.mean(), usum)
+
+
+def test_snis_numerator_and_denominator_are_unbiased():
+    """Averaged over hash draws, sum_{S∪T} w~/u v and sum_{S∪T} w~/u are unbiased for
+    the full sums (Eq. 9 with P[i in S] = u_i), so their ratio tends to Eq. 1."""
+    rng = np.random.default_rng(7)
+    d, n, K, L, s, w = 8, 200, 2, 12, 2, 6
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    exact = O.exact_attention(q, keys, vals)
+    ref = float((keys @ q).max() / math.sqrt(d))
+    nums, dens = [], []
+    for _ in range(1500):
+        W = rng.normal(size=(d, K * L))
+        t = O.HeadTables(keys, W, K, L, s, n)
+        r = O.decode_head(q, keys, vals, t, n, w)
+        num, den = O.snis_sums(q, keys, vals, r["S"], r["u"], r["T"], ref)
+        nums.append(num)
+        dens.append(den)
+    nums, dens = np.array(nums), np.array(dens)
+    full_logit = keys @ q / math.sqrt(d) - ref
+    np.testing.assert_allclose(dens.mean(), np.exp(full_logit).sum(),
+                               rtol=4 * dens.std(ddof=1) / math.sqrt(len(dens)) / dens.mean())
+    ratio = nums.mean(0) / dens.mean()
+    resid = nums - ratio[None, :] * dens[:, None]
+    se = resid.std(axis=0, ddof=1) / math.sqrt(len(dens)) / dens.mean()
+    assert np.all(np.abs(ratio - exact) < 4.5 * se + 1e-9), (ratio, exact, se)
+
+
+# ----------------------------------------------------------------------------------
+# a7 - a9 special cases that reduce to exact attention (Eq. 1)
+# ----------------------------------------------------------------------------------
+
+def test_every_key_sampled_when_K_is_zero_gives_exact_attention():
+    rng = np.random.default_rng(2)
+    d, n, L, s, w = 16, 97, 5, 4, 8
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    t = O.HeadTables(keys, np.zeros((d, 0)), 0, L, s, n)
+    r = O.decode_head(q, keys, vals, t, n, w)
+    np.testing.assert_array_equal(r["S"], np.arange(s, n - w))
+    np.testing.assert_allclose(r["u"], 1.0)
+    want = softmax(keys @ q / math.sqrt(d)) @ vals
+    np.testing.assert_allclose(r["out"], want, rtol=1e-12)
+    np.testing.assert_allclose(O.exact_attention(q, keys, vals), want, rtol=1e-12)
+
+
+def test_short_sequence_is_all_static_and_exact():
+    rng = np.random.default_rng(4)
+    d, n, K, L, s, w = 8, 50, 4, 6, 4, 64
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    t = O.HeadTables(keys, rng.normal(size=(d, K * L)), K, L, s, n)
+    r = O.decode_head(q, keys, vals, t, n, w)
+    assert len(r["S"]) == 0 and len(r["T"]) == n
+    np.testing.assert_allclose(r["out"], softmax(keys @ q / math.sqrt(d)) @ vals, rtol=1e-12)
+
+
+def test_translation_of_all_keys_changes_nothing():
+    """Softmax is translation invariant and keys are centered (MagicPIG §4.3)."""
+    rng = np.random.default_rng(9)
+    d, n, K, L, s, w = 16, 600, 4, 20, 4, 32
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    shift = 5 * rng.normal(size=d)
+    a = O.decode_head(q, keys, vals, O.HeadTables(keys, W, K, L, s, n), n, w)
+    b = O.decode_head(q, keys + shift, vals, O.HeadTables(keys + shift, W, K, L, s, n), n, w)
+    np.testing.assert_array_equal(a["S"], b["S"])
+    assert len(a["S"]) > 0
+    np.testing.assert_allclose(a["u"], b["u"], rtol=1e-10)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-9)
