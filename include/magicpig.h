@@ -1,0 +1,208 @@
+/*
+ * magicpig.h — C ABI of an LSH-sampled sparse decode-attention library for one
+ * GB300 GPU (sm_103a).
+ *
+ * The method is the one of "MagicPIG: LSH Sampling for Efficient LLM Generation"
+ * (arXiv 2410.16179v2):
+ *   - keys are centered by their mean before hashing (§4.3 "Data pre-processing");
+ *   - each key and each query gets L SimHash codes of K bits from K·L random
+ *     projections W ∈ R^{d×(K·L)} (§2.2 SimHash; §4.3 "Hash function selection";
+ *     Algorithm 1 'Encode');
+ *   - a key is sampled when its code equals the query's in at least two tables
+ *     (§4.3; Algorithm 1 'Query');
+ *   - the output is the self-normalised importance-sampling estimate
+ *     softmax(q·k/√d − log u) V over the sampled keys, with
+ *     u = 1 − (1 − p^K)^L − L p^K (1 − p^K)^(L−1), p = 1 − θ(q, k)/π (Eq. 9–11);
+ *   - sink tokens and a local window are attended exactly with u = 1 (§4.4
+ *     "On-device cache"; §5.1 Baselines: 4 sinks and a 64-token window).
+ *
+ * Tensor layouts (all row-major, C order, dense):
+ *   keys, values : [layers][batch][kv_heads][capacity][head_dim]   (the pages' K, V ∈ R^{n×d} per head)
+ *   q            : [layers][batch][q_heads][head_dim]              (the pages' q ∈ R^{1×d} per head)
+ *   W            : [layers or 1][head_dim][K·L] float32            (the pages' W ∈ R^{d×(K·L)})
+ *   out          : [layers][batch][q_heads][head_dim] float32
+ * Query head j of a sequence reads KV head j / (q_heads / kv_heads) (grouped-query attention).
+ * Element type of keys, values and q: MP_DTYPE_BF16 or MP_DTYPE_F32 (config.dtype).
+ *
+ * Ownership: every pointer passed in is owned by the caller. Device pointers must
+ * be device memory of the current device; the library allocates and frees nothing,
+ * never synchronises (except mp_get_status) and enqueues all work on the caller's
+ * stream (`stream` is a cudaStream_t; NULL is the legacy default stream).
+ *
+ * Errors: every call returns MP_OK (0) or a negative MP_ERR_* code and enqueues
+ * nothing when it fails validation. Faults detected by kernels while they run are
+ * ORed into a device status word kept in the tables (MP_STATUS_* bits), read with
+ * mp_get_status.
+ */
+#ifndef MAGICPIG_H_
+#define MAGICPIG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MP_API __attribute__((visibility("default")))
+#else
+#define MP_API
+#endif
+
+#define MP_ABI_VERSION 1
+
+/* return codes */
+#define MP_OK 0
+#define MP_ERR_INVALID_ARG (-1) /* null pointer, bad shape, inconsistent config */
+#define MP_ERR_UNSUPPORTED (-2) /* valid but not implemented (e.g. head_dim not 64/128) */
+#define MP_ERR_CAPACITY (-3)    /* a token index or length beyond config.capacity */
+#define MP_ERR_CUDA (-4)        /* a CUDA runtime call or kernel launch failed */
+#define MP_ERR_INJECTED (-5)    /* failure injected on the host by MP_FAULT_INJECT */
+#define MP_ERR_SCRATCH (-6)     /* scratch buffer smaller than required */
+
+/* device status bits (mp_get_status) */
+#define MP_STATUS_W_NOT_BF16 0x1u   /* bf16 path: a W entry was not bf16-representable */
+#define MP_STATUS_WAIT_TIMEOUT 0x2u /* a bounded wait on an mbarrier gave up */
+#define MP_STATUS_APPEND_GAP 0x4u   /* decode needed codes of a token never appended */
+#define MP_STATUS_NOT_BUILT 0x8u    /* decode or append on tables that were never built */
+
+/* element types */
+#define MP_DTYPE_F32 0
+#define MP_DTYPE_BF16 1
+
+/* how the sampled set is found */
+#define MP_MATCH_AUTO 0 /* choose by bytes moved per query */
+#define MP_MATCH_CSR 1  /* bucketed tables: one id list per (KV head, table, code) */
+
+typedef struct mp_config {
+  int32_t layers;      /* independent attention layers handled by one call */
+  int32_t batch;       /* independent sequences */
+  int32_t kv_heads;    /* KV heads per sequence */
+  int32_t q_heads;     /* query heads per sequence, a multiple of kv_heads */
+  int32_t head_dim;    /* d: 64 or 128 */
+  int32_t K;           /* bits per table, 0..12 (0: every key collides in every table) */
+  int32_t L;           /* tables, 1..1024 */
+  int32_t n_sink;      /* initial tokens always attended exactly (pages: 4) */
+  int32_t window;      /* most recent tokens always attended exactly (pages: 64) */
+  int32_t capacity;    /* maximum tokens per sequence (prefill + appended), <= 2^19 */
+  int32_t dtype;       /* MP_DTYPE_BF16 or MP_DTYPE_F32 (keys, values, q) */
+  int32_t w_per_layer; /* 1: W holds one matrix per layer; 0: one matrix shared by all layers */
+  int32_t match_mode;  /* MP_MATCH_AUTO or MP_MATCH_CSR */
+  int32_t threshold;   /* minimum colliding tables for a key to be sampled: 1 or 2 (pages: 2) */
+  int32_t reserved[4]; /* must be zero */
+} mp_config;
+
+/* Byte offsets (from the start of the tables buffer) of the arrays the library keeps
+ * between calls. U = layers·batch·kv_heads units, KLp = K·L rounded up to 256,
+ * NB = 2^K buckets. Exposed for tests and tools; the contents are library-private. */
+typedef struct mp_tables_layout {
+  uint64_t total_bytes;
+  uint64_t header;       /* 256 B: magic, prefill length, appended length, status word */
+  uint64_t center;       /* float [U][d]: mean key of tokens [n_sink, n_prefill) */
+  uint64_t beta;         /* float [U][KLp]: W^T · center */
+  uint64_t wt_f32;       /* float [layers or 1][KLp][d]: W transposed, zero-padded */
+  uint64_t wt_bf16;      /* bf16  [layers or 1][KLp][d] (bf16 configs only, else 0) */
+  uint64_t center_parts; /* float [U][parts][d]: partial sums while building */
+  uint64_t codes;        /* uint16 [U][L][capacity]: code of every hashed token, table-major */
+  uint64_t csr_offsets;  /* uint32 [U][L][NB+1]: bucket starts in csr_ids, per table */
+  uint64_t csr_ids;      /* uint32 [U][L][capacity]: token ids of [n_sink, n_prefill) by bucket, ascending */
+  int32_t kl_padded;
+  int32_t n_buckets;
+  int32_t parts;
+  int32_t reserved;
+} mp_tables_layout;
+
+/* Byte offsets in the decode scratch buffer. Q = layers·batch·q_heads. */
+typedef struct mp_decode_layout {
+  uint64_t total_bytes;
+  uint64_t q_codes;      /* uint16 [Q][L]: query codes */
+  uint64_t list_len;     /* int32 [Q]: entries in the list (sampled + exact) */
+  uint64_t sample_count; /* int32 [Q]: sampled entries |S| (they come first) */
+  uint64_t lists;        /* uint32 [Q][capacity]: token ids, S ascending then exact tokens
+                            (bit 31 set on exact tokens) */
+  uint64_t partials;     /* float [Q][splits_max][d+2]: split-K partial (m, l, acc[d]) */
+  uint64_t counters;     /* uint32 [Q]: split-K completion counters */
+  int32_t splits_max;
+  int32_t reserved;
+} mp_decode_layout;
+
+/* Validate a configuration. MP_OK or MP_ERR_INVALID_ARG / MP_ERR_UNSUPPORTED. */
+MP_API int mp_config_check(const mp_config* cfg);
+
+/* Layout and size of the tables buffer (device memory the caller allocates, at least
+ * 256-byte aligned; contents need no initialisation). */
+MP_API int mp_tables_layout_get(const mp_config* cfg, mp_tables_layout* out);
+
+/* Layout and size of the decode scratch buffer (device memory, 256-byte aligned,
+ * no initialisation needed; reusable across calls on the same stream). */
+MP_API int mp_decode_layout_get(const mp_config* cfg, mp_decode_layout* out);
+
+/* Build the hash tables from the prefill keys [0, n_prefill) of every
+ * (layer, sequence, KV head): center with the mean of keys [n_sink, n_prefill)
+ * (§4.3 "Data pre-processing"), SimHash every prefill key into L K-bit codes with
+ * the projections W (§2.2, §4.3, Algorithm 1 'Encode'; on bf16 keys the projection
+ * runs on tensor cores and W must be bf16-representable, else MP_STATUS_W_NOT_BF16),
+ * and bucket the ids of tokens [n_sink, n_prefill) per (head, table, code) —
+ * the hash tables HT of Algorithm 1.
+ *   keys    : device, layout above; rows [0, n_prefill) are read.
+ *   W       : device float32, [layers or 1][d][K·L] per config.w_per_layer.
+ *   tables  : device, mp_tables_layout_get(cfg).total_bytes.
+ * 1 <= n_prefill <= capacity, else MP_ERR_CAPACITY. Resets the status word. */
+MP_API int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill,
+                    const float* W, void* tables, void* stream);
+
+/* Hash the key at token index `pos` of every (layer, sequence, KV head) into all
+ * L tables (one decode-step append). The caller has already written
+ * keys[..][pos][:]. Uses the center fixed at build time. Tokens appended this way
+ * are matched by comparing stored codes once they leave the window.
+ * n_prefill <= pos < capacity, else MP_ERR_CAPACITY. */
+MP_API int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream);
+
+/* One decode step for every query head (Algorithm 1 with the exact sink/window
+ * cache of §4.4): hash q (uncentered), collect S = {i in [n_sink, n - window) :
+ * code equal in >= threshold tables}, and write
+ *   out = softmax([q·k_S/√d − log u_S, q·k_T/√d]) [V_S; V_T]
+ * with T the sinks [0, n_sink) and the window [n - window, n), u = 1 on T.
+ *   keys, values : device, layout above; rows [0, n) are read.
+ *   n            : tokens visible to the query, 1 <= n <= capacity.
+ *   q            : device [layers][batch][q_heads][d] in config.dtype.
+ *   out          : device float32 [layers][batch][q_heads][d].
+ *   scratch      : device, at least mp_decode_layout_get(cfg).total_bytes (scratch_bytes).
+ * Writes only out, scratch and the status word of tables. */
+MP_API int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys,
+                        const void* values, int32_t n, const void* q, float* out,
+                        void* scratch, size_t scratch_bytes, void* stream);
+
+/* Copy the device status word to *status (synchronises `stream`). */
+MP_API int mp_get_status(const void* tables, uint32_t* status, void* stream);
+
+/* Human-readable name of a return code. */
+MP_API const char* mp_status_string(int code);
+
+/* MP_ABI_VERSION of the loaded library. */
+MP_API int mp_abi_version(void);
+
+/* ---- measurement instrumentation (no counterpart on the pages) ----
+ * When enabled, every kernel launch of the calls above is bracketed by a pair of
+ * CUDA events recorded on the caller's stream. mp_profile_read synchronises those
+ * events, returns per-kernel launch counts and summed device time, and clears the
+ * record. Disabled by default; enabling it adds two event records per launch. */
+typedef struct mp_kernel_time {
+  char name[32];
+  int32_t launches;
+  int32_t reserved;
+  double total_ms;
+} mp_kernel_time;
+
+/* on = 1 starts recording (clearing earlier records), on = 0 stops. */
+MP_API int mp_profile_enable(int on);
+
+/* Writes up to `capacity` entries (one per kernel name seen) and their number to *count. */
+MP_API int mp_profile_read(mp_kernel_time* out, int32_t capacity, int32_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAGICPIG_H_ */

@@ -1,0 +1,486 @@
+// Host side of the C ABI: validation, buffer layouts and the launch sequence of
+// each call. No device memory is allocated here; every buffer is the caller's.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "mp_internal.h"
+
+namespace mp {
+
+static uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255u); }
+
+static int check_config(const mp_config* c) {
+  if (!c) return MP_ERR_INVALID_ARG;
+  if (c->layers < 1 || c->batch < 1 || c->kv_heads < 1 || c->q_heads < 1) return MP_ERR_INVALID_ARG;
+  if (c->q_heads % c->kv_heads != 0) return MP_ERR_INVALID_ARG;
+  if (c->K < 0 || c->L < 1 || c->n_sink < 0 || c->window < 0 || c->capacity < 1) return MP_ERR_INVALID_ARG;
+  if (c->dtype != MP_DTYPE_F32 && c->dtype != MP_DTYPE_BF16) return MP_ERR_INVALID_ARG;
+  if (c->w_per_layer != 0 && c->w_per_layer != 1) return MP_ERR_INVALID_ARG;
+  if (c->match_mode != MP_MATCH_AUTO && c->match_mode != MP_MATCH_CSR) return MP_ERR_INVALID_ARG;
+  if (c->threshold < 1 || c->threshold > c->L) return MP_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
+  if (c->head_dim != 64 && c->head_dim != 128) return MP_ERR_UNSUPPORTED;
+  if (c->K > kMaxK || c->L > kMaxL || c->capacity > kMaxCapacity) return MP_ERR_UNSUPPORTED;
+  if (c->threshold > 2) return MP_ERR_UNSUPPORTED;
+  // grid limits: units and queries index blockIdx.x / y
+  const int64_t q = int64_t(c->layers) * c->batch * c->q_heads;
+  if (q > (1 << 30)) return MP_ERR_UNSUPPORTED;
+  return MP_OK;
+}
+
+static Geometry geometry(const mp_config* c) {
+  Geometry g;
+  g.layers = c->layers;
+  g.batch = c->batch;
+  g.kvh = c->kv_heads;
+  g.qh = c->q_heads;
+  g.d = c->head_dim;
+  g.K = c->K;
+  g.L = c->L;
+  g.s = c->n_sink;
+  g.w = c->window;
+  g.cap = c->capacity;
+  g.dtype = c->dtype;
+  g.w_per_layer = c->w_per_layer;
+  g.threshold = c->threshold;
+  g.group = c->q_heads / c->kv_heads;
+  g.units = c->layers * c->batch * c->kv_heads;
+  g.queries = c->layers * c->batch * c->q_heads;
+  g.kl = c->K * c->L;
+  g.klp = int(align256(uint64_t(g.kl)));
+  if (g.klp == 0) g.klp = 256;
+  g.nb = 1 << c->K;
+  g.parts = 32;
+  g.n_w = c->w_per_layer ? c->layers : 1;
+  return g;
+}
+
+static void tables_layout(const Geometry& g, mp_tables_layout* o) {
+  std::memset(o, 0, sizeof(*o));
+  const uint64_t U = uint64_t(g.units), d = uint64_t(g.d), L = uint64_t(g.L), cap = uint64_t(g.cap);
+  uint64_t off = 0;
+  o->header = off;
+  off += 256;
+  o->center = off;
+  off = align256(off + U * d * 4);
+  o->beta = off;
+  off = align256(off + U * uint64_t(g.klp) * 4);
+  o->wt_f32 = off;
+  off = align256(off + uint64_t(g.n_w) * g.klp * d * 4);
+  if (g.dtype == MP_DTYPE_BF16) {
+    o->wt_bf16 = off;
+    off = align256(off + uint64_t(g.n_w) * g.klp * d * 2);
+  }
+  o->center_parts = off;
+  off = align256(off + U * uint64_t(g.parts) * d * 4);
+  o->codes = off;
+  off = align256(off + U * L * cap * 2);
+  o->csr_offsets = off;
+  off = align256(off + U * L * (uint64_t(g.nb) + 1) * 4);
+  o->csr_ids = off;
+  off = align256(off + U * L * cap * 4);
+  o->total_bytes = off;
+  o->kl_padded = g.klp;
+  o->n_buckets = g.nb;
+  o->parts = g.parts;
+}
+
+static void decode_layout(const Geometry& g, mp_decode_layout* o) {
+  std::memset(o, 0, sizeof(*o));
+  const uint64_t Q = uint64_t(g.queries);
+  uint64_t off = 0;
+  o->q_codes = off;
+  off = align256(off + Q * g.L * 2);
+  o->list_len = off;
+  off = align256(off + Q * 4);
+  o->sample_count = off;
+  off = align256(off + Q * 4);
+  o->lists = off;
+  off = align256(off + Q * uint64_t(g.cap) * 4);
+  o->partials = off;
+  off = align256(off + Q * kSplitsMax * uint64_t(g.d + 2) * 4);
+  o->counters = off;
+  off = align256(off + Q * 4);
+  o->total_bytes = off;
+  o->splits_max = kSplitsMax;
+}
+
+static TablesPtrs tables_ptrs(const Geometry& g, void* base) {
+  mp_tables_layout l;
+  tables_layout(g, &l);
+  char* b = static_cast<char*>(base);
+  TablesPtrs t;
+  t.hdr = reinterpret_cast<DevHeader*>(b + l.header);
+  t.center = reinterpret_cast<float*>(b + l.center);
+  t.beta = reinterpret_cast<float*>(b + l.beta);
+  t.wt32 = reinterpret_cast<float*>(b + l.wt_f32);
+  t.wt16 = l.wt_bf16 ? reinterpret_cast<__nv_bfloat16*>(b + l.wt_bf16) : nullptr;
+  t.cparts = reinterpret_cast<float*>(b + l.center_parts);
+  t.codes = reinterpret_cast<uint16_t*>(b + l.codes);
+  t.off = reinterpret_cast<uint32_t*>(b + l.csr_offsets);
+  t.ids = reinterpret_cast<uint32_t*>(b + l.csr_ids);
+  return t;
+}
+
+static DecodePtrs decode_ptrs(const Geometry& g, void* base) {
+  mp_decode_layout l;
+  decode_layout(g, &l);
+  char* b = static_cast<char*>(base);
+  DecodePtrs p;
+  p.qcodes = reinterpret_cast<uint16_t*>(b + l.q_codes);
+  p.list_len = reinterpret_cast<int32_t*>(b + l.list_len);
+  p.sample_count = reinterpret_cast<int32_t*>(b + l.sample_count);
+  p.lists = reinterpret_cast<uint32_t*>(b + l.lists);
+  p.partials = reinterpret_cast<float*>(b + l.partials);
+  p.counters = reinterpret_cast<uint32_t*>(b + l.counters);
+  return p;
+}
+
+// MP_FAULT_INJECT=build|append|decode|all makes the named calls fail before any
+// launch (host-side fault injection for error-path tests).
+static bool injected(const char* what) {
+  const char* e = std::getenv("MP_FAULT_INJECT");
+  if (!e || !*e) return false;
+  return std::strcmp(e, "all") == 0 || std::strcmp(e, what) == 0;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+// Hash path for bf16 keys at build time: tensor cores unless MP_HASH_PATH=simt.
+static bool use_simt_hash() {
+  const char* e = std::getenv("MP_HASH_PATH");
+  return e && std::strcmp(e, "simt") == 0;
+}
+
+// Number of split-K slices per query head: enough CTAs to fill the GPU a few times
+// over, but no slice shorter than about 128 list entries (estimated from the
+// closed-form budget at p = 1/2).
+static int choose_splits(const Geometry& g, int n) {
+  const double x = std::ldexp(1.0, -g.K);
+  double frac;
+  if (g.threshold == 1) frac = 1.0 - std::pow(1.0 - x, g.L);
+  else frac = 1.0 - std::pow(1.0 - x, g.L) - g.L * x * std::pow(1.0 - x, g.L - 1);
+  const int lo = std::min(g.s, n);
+  const int hi = std::max(lo, n - g.w);
+  const double est = double(n - (hi - lo)) + frac * double(hi - lo);
+  const int by_len = int(std::ceil(est / 128.0));
+  const int target = 8 * device_sm_count();
+  const int by_fill = (target + g.queries - 1) / g.queries;
+  int s = std::min(by_len, by_fill);
+  if (s < 1) s = 1;
+  if (s > kSplitsMax) s = kSplitsMax;
+  return s;
+}
+
+// ---- optional per-launch event timing ----
+enum KernelId {
+  K_PREPARE_W, K_CENTER, K_HASH_KEYS_SIMT, K_HASH_KEYS_TC, K_CSR_BUILD, K_HASH_APPEND, K_MARK_APPENDED,
+  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_COUNT
+};
+static const char* kKernelNames[K_COUNT] = {"prepare_w", "center", "hash_keys_simt", "hash_keys_tc",
+                                            "csr_build", "hash_append", "mark_appended", "hash_query",
+                                            "match_csr", "attend"};
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRec> g_prof;
+static std::vector<cudaEvent_t> g_pool;
+
+static cudaEvent_t pool_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launcher call with events when profiling is on.
+class ProfScope {
+ public:
+  ProfScope(cudaStream_t st, int id) : st_(st), id_(id) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!g_prof_on) return;
+    a_ = pool_event();
+    b_ = pool_event();
+    if (a_ && b_) cudaEventRecord(a_, st_);
+  }
+  ~ProfScope() {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!a_ || !b_) return;
+    cudaEventRecord(b_, st_);
+    g_prof.push_back({id_, a_, b_});
+  }
+
+ private:
+  cudaStream_t st_;
+  int id_;
+  cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+}  // namespace mp
+
+using namespace mp;
+
+extern "C" {
+
+int mp_abi_version(void) { return MP_ABI_VERSION; }
+
+const char* mp_status_string(int code) {
+  switch (code) {
+    case MP_OK: return "ok";
+    case MP_ERR_INVALID_ARG: return "invalid argument";
+    case MP_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MP_ERR_CAPACITY: return "token index or length beyond capacity";
+    case MP_ERR_CUDA: return "CUDA error";
+    case MP_ERR_INJECTED: return "injected failure";
+    case MP_ERR_SCRATCH: return "scratch buffer too small";
+    default: return "unknown error";
+  }
+}
+
+int mp_config_check(const mp_config* cfg) { return check_config(cfg); }
+
+int mp_tables_layout_get(const mp_config* cfg, mp_tables_layout* out) {
+  const int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!out) return MP_ERR_INVALID_ARG;
+  tables_layout(geometry(cfg), out);
+  return MP_OK;
+}
+
+int mp_decode_layout_get(const mp_config* cfg, mp_decode_layout* out) {
+  const int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!out) return MP_ERR_INVALID_ARG;
+  decode_layout(geometry(cfg), out);
+  return MP_OK;
+}
+
+int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, const float* W,
+                    void* tables, void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!keys || !W || !tables) return MP_ERR_INVALID_ARG;
+  if (!aligned16(keys) || !aligned16(W) || (reinterpret_cast<uintptr_t>(tables) & 255u))
+    return MP_ERR_INVALID_ARG;
+  if (n_prefill < 1 || n_prefill > cfg->capacity) return MP_ERR_CAPACITY;
+  if (injected("build")) return MP_ERR_INJECTED;
+  const Geometry g = geometry(cfg);
+  const TablesPtrs t = tables_ptrs(g, tables);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();  // clear a stale error so that it is not blamed on this call
+  if (cudaMemsetAsync(t.hdr, 0, sizeof(DevHeader), st) != cudaSuccess) return MP_ERR_CUDA;
+  {
+    ProfScope ps(st, K_PREPARE_W);
+    if (launch_prepare_w(g, W, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  {
+    ProfScope ps(st, K_CENTER);
+    if (launch_center(g, keys, n_prefill, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  bool done = false;
+  if (g.dtype == MP_DTYPE_BF16 && !use_simt_hash()) {
+    ProfScope ps(st, K_HASH_KEYS_TC);
+    if (launch_hash_keys_tc(g, keys, n_prefill, t, st, &done) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  if (!done) {
+    HashRowsArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.src = keys;
+    a.src_gs = int64_t(g.cap) * g.d;
+    a.src_rs = g.d;
+    a.rows = n_prefill;
+    a.groups = g.units;
+    a.row0 = 0;
+    a.center = t.center;
+    a.c_gs = 1;
+    a.c_rs = 0;
+    a.wt32 = t.wt32;
+    a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+    a.groups_per_w = g.batch * g.kvh;
+    a.out = t.codes;
+    a.out_gs = int64_t(g.L) * g.cap;
+    a.out_rs = 1;
+    a.out_ts = g.cap;
+    ProfScope ps(st, K_HASH_KEYS_SIMT);
+    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  {
+    ProfScope ps(st, K_CSR_BUILD);
+    if (launch_csr_build(g, n_prefill, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!keys || !tables) return MP_ERR_INVALID_ARG;
+  if (!aligned16(keys) || (reinterpret_cast<uintptr_t>(tables) & 255u)) return MP_ERR_INVALID_ARG;
+  if (pos < 0 || pos >= cfg->capacity) return MP_ERR_CAPACITY;
+  if (injected("append")) return MP_ERR_INJECTED;
+  const Geometry g = geometry(cfg);
+  const TablesPtrs t = tables_ptrs(g, tables);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  HashRowsArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.src = keys;
+  a.src_gs = int64_t(g.batch) * g.kvh * g.cap * g.d;  // one group per layer
+  a.src_rs = int64_t(g.cap) * g.d;                     // one row per (sequence, KV head)
+  a.rows = g.batch * g.kvh;
+  a.groups = g.layers;
+  a.row0 = 0;
+  a.center = t.center;
+  a.c_gs = g.batch * g.kvh;
+  a.c_rs = 1;
+  a.wt32 = t.wt32;
+  a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+  a.groups_per_w = 1;
+  a.out = t.codes;
+  a.out_gs = int64_t(g.batch) * g.kvh * g.L * g.cap;
+  a.out_rs = int64_t(g.L) * g.cap;
+  a.out_ts = g.cap;
+  // the row index addresses (sequence, KV head); the token is `pos`
+  a.src = static_cast<const char*>(keys) + int64_t(pos) * g.d * (g.dtype == MP_DTYPE_BF16 ? 2 : 4);
+  a.out = t.codes + pos;
+  {
+    ProfScope ps(st, K_HASH_APPEND);
+    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  {
+    ProfScope ps(st, K_MARK_APPENDED);
+    if (launch_mark_appended(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, const void* values,
+                        int32_t n, const void* q, float* out, void* scratch, size_t scratch_bytes,
+                        void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!tables || !keys || !values || !q || !out || !scratch) return MP_ERR_INVALID_ARG;
+  if (!aligned16(keys) || !aligned16(values) || !aligned16(q) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(tables) & 255u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
+    return MP_ERR_INVALID_ARG;
+  if (n < 1 || n > cfg->capacity) return MP_ERR_CAPACITY;
+  const Geometry g = geometry(cfg);
+  mp_decode_layout dl;
+  decode_layout(g, &dl);
+  if (scratch_bytes < dl.total_bytes) return MP_ERR_SCRATCH;
+  if (injected("decode")) return MP_ERR_INJECTED;
+  const TablesPtrs t = tables_ptrs(g, tables);
+  const DecodePtrs dp = decode_ptrs(g, scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  // 1. query codes (Algorithm 1 'Encode'); the query is not centered
+  HashRowsArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.src = q;
+  a.src_gs = int64_t(g.batch) * g.qh * g.d;
+  a.src_rs = g.d;
+  a.rows = g.batch * g.qh;
+  a.groups = g.layers;
+  a.row0 = 0;
+  a.center = nullptr;
+  a.wt32 = t.wt32;
+  a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+  a.groups_per_w = 1;
+  a.out = dp.qcodes;
+  a.out_gs = int64_t(g.batch) * g.qh * g.L;
+  a.out_rs = g.L;
+  a.out_ts = 1;
+  {
+    ProfScope ps(st, K_HASH_QUERY);
+    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  // 2. sampled set (Algorithm 1 'Query') + exact tokens
+  {
+    ProfScope ps(st, K_MATCH_CSR);
+    if (launch_match_csr(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  // 3. split-K importance-weighted attention with fused combine
+  const int splits = choose_splits(g, n);
+  {
+    ProfScope ps(st, K_ATTEND);
+    if (launch_attend(g, n, splits, t, keys, values, q, out, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+int mp_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  g_prof_on = on != 0;
+  return MP_OK;
+}
+
+int mp_profile_read(mp_kernel_time* out, int32_t capacity, int32_t* count) {
+  if (!count || (capacity > 0 && !out)) return MP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  double ms[K_COUNT] = {0};
+  int n[K_COUNT] = {0};
+  int rc = MP_OK;
+  for (auto& r : g_prof) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      rc = MP_ERR_CUDA;
+    ms[r.id] += t;
+    n[r.id] += 1;
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  int k = 0;
+  for (int i = 0; i < K_COUNT; ++i) {
+    if (n[i] == 0) continue;
+    if (k < capacity) {
+      std::memset(&out[k], 0, sizeof(out[k]));
+      std::strncpy(out[k].name, kKernelNames[i], sizeof(out[k].name) - 1);
+      out[k].launches = n[i];
+      out[k].total_ms = ms[i];
+    }
+    ++k;
+  }
+  *count = k;
+  return rc;
+}
+
+int mp_get_status(const void* tables, uint32_t* status, void* stream) {
+  if (!tables || !status) return MP_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const DevHeader* h = static_cast<const DevHeader*>(tables);
+  if (cudaMemcpyAsync(status, &h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MP_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MP_ERR_CUDA;
+  return MP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Internal declarations shared by the translation units of libmagicpig.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "magicpig.h"
+
+namespace mp {
+
+constexpr uint32_t kMagic = 0x4D504947u;  // "MPIG"
+constexpr int kMaxK = 12;
+constexpr int kMaxL = 1024;
+constexpr int kMaxCapacity = 1 << 19;
+constexpr int kSplitsMax = 64;
+constexpr uint32_t kExactFlag = 0x80000000u;
+
+// First 256 bytes of the tables buffer.
+struct DevHeader {
+  uint32_t magic;
+  int32_t n_prefill;     // tokens hashed at build time
+  int32_t appended_end;  // one past the last token whose code is stored
+  uint32_t status;       // MP_STATUS_* bits
+  int32_t pad[60];
+};
+static_assert(sizeof(DevHeader) == 256, "header size");
+
+// Sizes derived from an mp_config.
+struct Geometry {
+  int layers, batch, kvh, qh, d, K, L, s, w, cap, dtype, w_per_layer, threshold;
+  int group;    // q_heads / kv_heads
+  int units;    // layers * batch * kv_heads
+  int queries;  // layers * batch * q_heads
+  int kl, klp;  // K*L and K*L rounded up to 256
+  int nb;       // 2^K
+  int parts;    // partial sums per unit for the center
+  int n_w;      // number of W matrices
+};
+
+struct TablesPtrs {
+  DevHeader* hdr;
+  float* center;
+  float* beta;
+  float* wt32;
+  __nv_bfloat16* wt16;
+  float* cparts;
+  uint16_t* codes;
+  uint32_t* off;
+  uint32_t* ids;
+};
+
+struct DecodePtrs {
+  uint16_t* qcodes;
+  int32_t* list_len;
+  int32_t* sample_count;
+  uint32_t* lists;
+  float* partials;
+  uint32_t* counters;
+};
+
+// Rows to hash: row r (0-based) of group g lives at
+//   src + g*src_gs + (row0 + r)*src_rs          (elements)
+// and is centered with  center + (g*c_gs + r*c_rs)*d  (if center != nullptr).
+// Codes go to out + g*out_gs + (row0 + r)*out_rs + t*out_ts.
+struct HashRowsArgs {
+  const void* src;
+  int64_t src_gs, src_rs;
+  int rows, groups, row0;
+  const float* center;
+  int64_t c_gs, c_rs;
+  const float* wt32;      // [n_w][klp][d]
+  int64_t w_stride;       // floats between consecutive W matrices (0: shared)
+  int groups_per_w;       // group g uses W matrix g / groups_per_w
+  uint16_t* out;
+  int64_t out_gs, out_rs, out_ts;
+};
+
+// ---- launchers (each returns cudaError_t of the launch) ----
+cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,
+                          cudaStream_t st);
+cudaError_t launch_hash_rows(const Geometry& g, const HashRowsArgs& a, cudaStream_t st);
+cudaError_t launch_hash_keys_tc(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,
+                                cudaStream_t st, bool* used);
+cudaError_t launch_csr_build(const Geometry& g, int n_prefill, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_mark_appended(const Geometry& g, int pos, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp,
+                             cudaStream_t st);
+cudaError_t launch_attend(const Geometry& g, int n, int splits, const TablesPtrs& t, const void* keys,
+                          const void* values, const void* q, float* out, const DecodePtrs& dp,
+                          cudaStream_t st);
+
+int device_sm_count();
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+#endif
+
+}  // namespace mp

@@ -1,0 +1,114 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+entry point, validates arguments and injects faults on the host before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "magicpig.h")
+
+
+@pytest.fixture(scope="module")
+def mp():
+    import __graft_entry__
+    __graft_entry__.build()
+    import lsh_sampled_sparse_centered_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"MP_API\s+[\w\s\*]+?\b(mp_\w+)\s*\(", src)
+
+
+def test_every_declared_symbol_is_exported(mp):
+    names = _declared()
+    assert len(names) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", mp.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s+(mp_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(mp.LIB_PATH)
+    for n in names:
+        assert getattr(lib, n) is not None
+    assert set(mp.EXPORTED) <= set(names)
+    assert mp.mp_abi_version() == 1
+
+
+def _cfg(mp, **kw):
+    base = dict(layers=1, batch=1, kv_heads=2, q_heads=4, head_dim=128, K=8, L=75, n_sink=4, window=64,
+                capacity=4096, dtype="bf16")
+    base.update(kw)
+    return mp.make_config(**base)
+
+
+def test_config_validation(mp):
+    assert mp.mp_config_check(_cfg(mp)) == mp.MP_OK
+    bad = [dict(q_heads=3), dict(layers=0), dict(K=-1), dict(L=0), dict(capacity=0), dict(dtype=7),
+           dict(threshold=0), dict(window=-1), dict(match_mode=9)]
+    for b in bad:
+        assert mp.mp_config_check(_cfg(mp, **b)) == mp.MP_ERR_INVALID_ARG, b
+    unsup = [dict(head_dim=96), dict(K=13), dict(L=2000), dict(capacity=(1 << 19) + 1), dict(threshold=3)]
+    for u in unsup:
+        assert mp.mp_config_check(_cfg(mp, **u)) == mp.MP_ERR_UNSUPPORTED, u
+    c = _cfg(mp)
+    c.reserved[2] = 1
+    assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
+
+
+def test_layouts_are_aligned_disjoint_and_sized(mp):
+    c = _cfg(mp, layers=2, w_per_layer=True)
+    t = mp.mp_tables_layout_get(c)
+    names = ["header", "center", "beta", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets", "csr_ids"]
+    offs = [getattr(t, n) for n in names]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and len(set(offs)) == len(offs)
+    U, L, cap, d = 2 * 1 * 2, 75, 4096, 128
+    assert t.csr_offsets - t.codes >= U * L * cap * 2
+    assert t.total_bytes - t.csr_ids >= U * L * cap * 4
+    assert t.kl_padded == 768 and t.n_buckets == 256
+    assert t.wt_bf16 - t.wt_f32 >= 2 * 768 * d * 4
+    dl = mp.mp_decode_layout_get(c)
+    Q = 2 * 4
+    assert dl.lists % 256 == 0 and dl.partials - dl.lists >= Q * cap * 4
+    assert dl.total_bytes - dl.counters >= Q * 4
+    f32 = mp.mp_tables_layout_get(_cfg(mp, dtype="f32"))
+    assert f32.wt_bf16 == 0
+
+
+def test_argument_errors_return_before_any_launch(mp):
+    c = _cfg(mp)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    assert mp.call_raw("mp_build_tables", ctypes.byref(c), None, 10, fake, fake, None) == mp.MP_ERR_INVALID_ARG
+    assert mp.call_raw("mp_build_tables", ctypes.byref(c), fake, 0, fake, fake, None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_build_tables", ctypes.byref(c), fake, 5000, fake, fake, None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_build_tables", ctypes.byref(c), fake + 8, 10, fake, fake, None) == mp.MP_ERR_INVALID_ARG
+    assert mp.call_raw("mp_append", ctypes.byref(c), fake, fake, 4096, None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_append", ctypes.byref(c), fake, fake, -1, None) == mp.MP_ERR_CAPACITY
+    dl = mp.mp_decode_layout_get(c)
+    assert mp.call_raw("mp_decode_attention", ctypes.byref(c), fake, fake, fake, 100, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes - 1), None) == mp.MP_ERR_SCRATCH
+    assert mp.call_raw("mp_decode_attention", ctypes.byref(c), fake, fake, fake, 0, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_decode_attention", ctypes.byref(c), fake, fake, None, 100, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_INVALID_ARG
+    assert mp.call_raw("mp_get_status", None, None, None) == mp.MP_ERR_INVALID_ARG
+    assert mp.mp_status_string(mp.MP_ERR_SCRATCH) == "scratch buffer too small"
+
+
+def test_fault_injection_on_the_host(mp, monkeypatch):
+    c = _cfg(mp)
+    fake = 1 << 20
+    dl = mp.mp_decode_layout_get(c)
+    monkeypatch.setenv("MP_FAULT_INJECT", "decode")
+    assert mp.call_raw("mp_decode_attention", ctypes.byref(c), fake, fake, fake, 100, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_INJECTED
+    monkeypatch.setenv("MP_FAULT_INJECT", "all")
+    assert mp.call_raw("mp_build_tables", ctypes.byref(c), fake, 10, fake, fake, None) == mp.MP_ERR_INJECTED
+    assert mp.call_raw("mp_append", ctypes.byref(c), fake, fake, 20, None) == mp.MP_ERR_INJECTED
+    with pytest.raises(mp.MagicPigError) as e:
+        mp.mp_append(c, fake, fake, 20, stream=0)
+    assert e.value.code == mp.MP_ERR_INJECTED

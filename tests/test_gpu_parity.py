@@ -1,0 +1,121 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, stage by stage
+(codes, bucket tables, query codes, sampled sets, exact tokens, outputs) on seeded
+synthetic workloads. Codes are compared bit-exactly except near-tie projections
+(|y| < 1e-5 ||x|| ||w_j||), which are counted; sampled sets exactly on the GPU's
+codes; outputs within 2e-3 relative L2 of the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from gpu_harness import GpuRun, check_workload, config_for, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import lsh_sampled_sparse_centered_gb300 as m
+    return m
+
+
+def _report(name, rep):
+    print(f"\n[{name}] heads={rep['heads']} max_rel_l2={rep['max_rel_l2']:.2e} "
+          f"sampled_frac={rep['sampled'] / max(1, rep['region']):.4f} codes_differ(near-tie)={rep['codes_differ']} "
+          f"q_codes_differ(near-tie)={rep['q_codes_differ']} S_differ_vs_oracle_codes={rep['S_differ_oracle_codes']}")
+
+
+def test_config0_tiny_fp32(mp):
+    wl = WL.WORKLOADS[0]
+    rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=wl.L)
+    _report("cfg0", rep)
+    assert rep["heads"] == 1
+
+
+def test_config1_llama8b_layer(mp):
+    wl = WL.WORKLOADS[1]
+    rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=8)
+    _report("cfg1", rep)
+    assert rep["heads"] == 32
+
+
+RAGGED = WL.Workload("ragged-appends", layers=2, batch=2, kv_heads=2, q_heads=8, head_dim=128,
+                     n_prefill=1037, steps=40, append=True, K=6, L=20, dtype="bf16", seed=17, window=16,
+                     w_per_layer=True)
+
+
+def test_ragged_appends_leave_the_window(mp):
+    """Appended tokens leave the window after 16 steps and are then matched from
+    the stored codes; prefill length not a multiple of any tile."""
+    rep = check_workload(mp, RAGGED, WL.generate(RAGGED), steps=[0, 15, 16, 17, 39], check_csr_tables=20)
+    _report("ragged", rep)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype="f32", head_dim=128, w_bf16=False),
+    dict(dtype="bf16", head_dim=64),
+    dict(dtype="f32", head_dim=64, q_heads=2, kv_heads=2, w_bf16=False),
+])
+def test_dtypes_and_head_dims(mp, kw):
+    wl = WL.Workload("dt", layers=1, batch=1, kv_heads=2, q_heads=4, head_dim=128, n_prefill=2500, steps=2,
+                     append=True, K=7, L=30, dtype="bf16", seed=23).replace(**kw)
+    rep = check_workload(mp, wl, WL.generate(wl))
+    _report(str(kw), rep)
+
+
+def test_threshold_one(mp):
+    wl = WL.Workload("t1", layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=128, n_prefill=3000, steps=1,
+                     append=False, K=10, L=12, dtype="bf16", seed=31)
+    rep = check_workload(mp, wl, WL.generate(wl), threshold=1)
+    _report("threshold1", rep)
+
+
+def test_K0_samples_everything_and_equals_exact_attention(mp):
+    wl = WL.Workload("k0", layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=128, n_prefill=700, steps=1,
+                     append=False, K=0, L=3, dtype="bf16", seed=5)
+    t = WL.generate(wl)
+    rep = check_workload(mp, wl, t)
+    assert rep["sampled"] == rep["region"]
+    run = GpuRun(mp, wl, t, "cuda:0")
+    run.build()
+    out = run.decode(0, 700).cpu().numpy()
+    k = t["keys"][0, 0, 0].double().numpy()
+    v = t["values"][0, 0, 0].double().numpy()
+    for j in range(2):
+        q = t["queries"][0, 0, 0, j].double().numpy()
+        lg = k @ q / np.sqrt(128)
+        e = np.exp(lg - lg.max())
+        assert rel_l2(out[0, 0, j], e @ v / e.sum()) < 2e-3
+
+
+def test_short_sequences_are_all_exact(mp):
+    wl = WL.Workload("short", layers=1, batch=2, kv_heads=1, q_heads=1, head_dim=64, n_prefill=3, steps=70,
+                     append=True, K=5, L=8, dtype="bf16", seed=9)
+    rep = check_workload(mp, wl, WL.generate(wl), steps=[0, 1, 60, 66, 67, 69])
+    _report("short", rep)
+
+
+def test_status_flags(mp):
+    wl = WL.Workload("st", layers=1, batch=1, kv_heads=1, q_heads=1, head_dim=128, n_prefill=300, steps=100,
+                     append=True, K=4, L=4, dtype="bf16", seed=3, window=8)
+    t = WL.generate(wl)
+    run = GpuRun(mp, wl, t, "cuda:0")
+    # decode on never-built tables
+    run.tables.zero_()
+    run.decode(0, 300)
+    assert run.status() & mp.MP_STATUS_NOT_BUILT
+    # W that bf16 cannot hold exactly
+    run.W += 1e-3 * torch.randn_like(run.W)
+    run.build()
+    assert run.status() == mp.MP_STATUS_W_NOT_BF16
+    # a clean build, then a decode that needs codes of tokens never appended
+    run.W.copy_(t["W"].to(run.W.device))
+    run.build()
+    run.decode(0, 300)
+    assert run.status() == 0
+    run.decode(0, 350)
+    assert run.status() == mp.MP_STATUS_APPEND_GAP

@@ -212,11 +212,10 @@ def query_block(wl: Workload, step: int, layer: int, b: int, device="cpu") -> to
     """Queries of all query heads of sequence ``b`` in ``layer`` at decode step
     ``step``, float64 [q_heads, d]; head j belongs to KV head j // group."""
     d = wl.head_dim
-    out = torch.empty(wl.q_heads, d, dtype=torch.float64, device=device)
-    for j in range(wl.q_heads):
-        mu = head_mu(wl, layer, b, j // wl.group, device)
-        out[j] = -2.0 * mu + gaussian(stream_key(wl.seed, P_QUERY, step, layer, b, j), d, device)
-    return out
+    mus = torch.stack([head_mu(wl, layer, b, h, device) for h in range(wl.kv_heads)])
+    noise = gaussian(stream_key(wl.seed, P_QUERY, step, layer, b), wl.q_heads * d, device).view(wl.q_heads, d)
+    idx = torch.arange(wl.q_heads, device=device) // wl.group
+    return noise - 2.0 * mus[idx]
 
 
 def projection(wl: Workload, layer: int, device="cpu") -> torch.Tensor:
