@@ -1,0 +1,530 @@
+#!/usr/bin/env python
+"""Benchmark of LSH-sampled decode attention (MagicPIG's hot path) on GB300.
+
+One step = one whole job of the Llama-3.1-8B-shaped long-context workload: build the
+hash tables of 32 layers x 8 KV heads from 96K prefill keys (center, SimHash on
+tensor cores, bucket), then 64 decode steps, each appending one key per KV head and
+answering all 32 x 32 query heads. Inputs are resident in HBM when timing starts
+(12.9 GB of K/V, larger than L2). `value` is queries answered per second by all
+ranks; the JSON line also carries per-kernel timings, the roofline of the dominant
+kernel, the CPU oracle's throughput on a bounded sample and an end-to-end figure
+with host buffers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LSH-sampled decode attention: μs/step, queries/s, achieved HBM GB/s vs roofline"
+DEFAULT_WORKLOAD = 2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="replay the decode steps from a CUDA graph")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+# ----------------------------------------------------------------------------------
+
+def dist_setup(use_cuda: bool):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if use_cuda:
+        torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, use_cuda: bool) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------
+# peaks and clocks
+# ----------------------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not self.path:
+            return None
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------
+
+class Job:
+    """Buffers of one workload replica on the current GPU and the ABI calls of one job."""
+
+    def __init__(self, mp, wl, device, stream):
+        import torch
+        import workloads as WL
+        self.mp, self.wl, self.dev, self.stream = mp, wl, device, stream
+        t = WL.generate(wl, device=device)
+        self.keys, self.values, self.W = t["keys"], t["values"], t["W"].contiguous()
+        self.queries = t["queries"]
+        self.cfg = mp.make_config(layers=wl.layers, batch=wl.batch, kv_heads=wl.kv_heads, q_heads=wl.q_heads,
+                                  head_dim=wl.head_dim, K=wl.K, L=wl.L, n_sink=wl.n_sink, window=wl.window,
+                                  capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer)
+        self.tl = mp.mp_tables_layout_get(self.cfg)
+        self.dl = mp.mp_decode_layout_get(self.cfg)
+        self.tables = torch.empty(self.tl.total_bytes, dtype=torch.uint8, device=device)
+        self.scratch = torch.empty(self.dl.total_bytes, dtype=torch.uint8, device=device)
+        self.outs = torch.empty(wl.steps, wl.layers, wl.batch, wl.q_heads, wl.head_dim, dtype=torch.float32,
+                                device=device)
+        self.sp = stream.cuda_stream
+        self.hook = None
+
+    def build(self, keys=None, W=None):
+        mp = self.mp
+        mp.mp_build_tables(self.cfg, self.keys if keys is None else keys, self.wl.n_prefill,
+                           self.W if W is None else W, self.tables, stream=self.sp)
+
+    def decode_steps(self, keys=None, values=None, queries=None):
+        mp, wl = self.mp, self.wl
+        k = self.keys if keys is None else keys
+        v = self.values if values is None else values
+        qs = self.queries if queries is None else queries
+        for s in range(wl.steps):
+            n = wl.seq_len(s)
+            if wl.append:
+                mp.mp_append(self.cfg, self.tables, k, n - 1, stream=self.sp)
+            mp.mp_decode_attention(self.cfg, self.tables, k, v, n, qs[s], self.outs[s], self.scratch,
+                                   scratch_bytes=self.dl.total_bytes, stream=self.sp)
+            if self.hook:
+                self.hook(s, n)
+
+    def run(self):
+        self.build()
+        self.decode_steps()
+
+    @property
+    def queries_per_job(self):
+        wl = self.wl
+        return wl.steps * wl.layers * wl.batch * wl.q_heads
+
+    @property
+    def launches_per_job(self):
+        # prepare_w, center (2 kernels), hash keys, csr build; per step: append hash + mark,
+        # query hash, match, attend
+        return 5 + self.wl.steps * (5 if self.wl.append else 3)
+
+
+def decode_state_stats(job, torch):
+    """Device-side sums used for algorithmic bytes: total list entries and sampled entries,
+    and the total bucket entries the match kernel walked."""
+    wl, dl, tl = job.wl, job.dl, job.tl
+    Q = wl.layers * wl.batch * wl.q_heads
+    U = wl.layers * wl.batch * wl.kv_heads
+    ln = job.scratch[dl.list_len: dl.list_len + 4 * Q].view(torch.int32).to(torch.int64)
+    ns = job.scratch[dl.sample_count: dl.sample_count + 4 * Q].view(torch.int32).to(torch.int64)
+    qc = (job.scratch[dl.q_codes: dl.q_codes + 2 * Q * wl.L].view(torch.int16).to(torch.int64) & 0xFFFF).view(Q, wl.L)
+    nb = tl.n_buckets
+    off = job.tables[tl.csr_offsets: tl.csr_offsets + 4 * U * wl.L * (nb + 1)].view(torch.int32).view(U, wl.L, nb + 1)
+    unit = torch.arange(Q, device=qc.device) // wl.group
+    t = torch.arange(wl.L, device=qc.device)
+    b0 = off[unit[:, None], t[None, :], qc].to(torch.int64)
+    b1 = off[unit[:, None], t[None, :], qc + 1].to(torch.int64)
+    return torch.stack([ln.sum(), ns.sum(), (b1 - b0).sum()])
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import workloads as WL
+    import __graft_entry__
+    __graft_entry__.build()
+    import lsh_sampled_sparse_centered_gb300 as mp
+
+    dev = torch.device("cuda", local)
+    wl = WL.WORKLOADS[args.workload]
+    wl = wl.replace(seed=wl.seed + 1000 * rank)  # independent replica per rank
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        job = Job(mp, wl, dev, stream)
+    torch.cuda.synchronize()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            job.run()
+    torch.cuda.synchronize()
+    assert mp.mp_get_status(job.tables, stream=job.sp) == 0
+
+    # timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                job.run()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, True)
+    clocks = clk.summary()
+
+    # per-kernel device time (events around each launch) + algorithmic sizes, one job
+    stats = torch.zeros(3, dtype=torch.int64, device=dev)
+
+    def hook(s, n):
+        stats.add_(decode_state_stats(job, torch))
+
+    job.hook = hook
+    mp.mp_profile_enable(True)
+    with torch.cuda.stream(stream):
+        job.run()
+    torch.cuda.synchronize()
+    prof = mp.mp_profile_read()
+    mp.mp_profile_enable(False)
+    job.hook = None
+    list_entries, sampled_entries, bucket_entries = [int(x) for x in stats.cpu()]
+
+    pk = peaks()
+    res = summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(job, stream, args, world)
+
+    queries = job.queries_per_job * args.steps * world
+    value = queries / (ms_max / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic: seeded cone keys k=3mu+N(0,I) with sink k0=-6mu, queries q=-2mu+N(0,I), "
+                "values N(0,1), W N(0,1) rounded to bf16",
+        "config": {"workload": wl.name, "layers": wl.layers, "batch": wl.batch, "kv_heads": wl.kv_heads,
+                   "q_heads": wl.q_heads, "head_dim": wl.head_dim, "n_prefill": wl.n_prefill,
+                   "decode_steps": wl.steps, "K": wl.K, "L": wl.L, "n_sink": wl.n_sink, "window": wl.window,
+                   "step": "build tables + %d x (append + decode attention)" % wl.steps,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (%.1f GB of K/V resident)" % (
+                       2 * job.keys.numel() * job.keys.element_size() / 1e9)},
+        "us_per_decode_step": res["us_per_decode_step"],
+        "build_ms": res["build_ms"],
+        "sampled_fraction": res["sampled_fraction"],
+        "closed_form_fraction": res["closed_form_fraction"],
+        "roofline": res["roofline"],
+        "pipeline_roofline": res["pipeline_roofline"],
+        "kernels": res["kernels"],
+        "gpu_launches": job.launches_per_job * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": None,
+    }
+    return line, job
+
+
+def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
+    """Per-kernel average durations and algorithmic work for one job; roofline of the
+    kernel with the largest share of device time."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    U = wl.layers * wl.batch * wl.kv_heads
+    Q = wl.layers * wl.batch * wl.q_heads
+    d, KL = wl.head_dim, wl.K * wl.L
+    n0, s = wl.n_prefill, wl.n_sink
+    steps = wl.steps
+    hbm = pk["hbm_gbs"]
+    tc = pk["bf16_tflops_sustained"]
+    work = {
+        # name: (kind, amount per job)   kind: "bytes" or "flops"
+        "prepare_w": ("bytes", (wl.layers if wl.w_per_layer else 1) * KL * d * (4 + 4 + esz)),
+        "center": ("bytes", U * (n0 - s) * d * esz),
+        "hash_keys_tc": ("flops", 2.0 * U * n0 * d * KL),
+        "hash_keys_simt": ("flops", 2.0 * U * n0 * d * KL),
+        "csr_build": ("bytes", U * wl.L * ((n0 - s) * (2 + 4) + (2 ** wl.K + 1) * 4)),
+        "hash_append": ("flops", 2.0 * steps * U * d * KL),
+        "mark_appended": ("bytes", 0),
+        "hash_query": ("flops", 2.0 * steps * Q * d * KL),
+        "match_csr": ("bytes", bucket_entries * 4 + steps * Q * wl.L * (8 + 2) + list_entries * 4),
+        "attend": ("bytes", list_entries * (2 * d * esz + 4) + steps * Q * d * (esz + 4)),
+    }
+    kernels = {}
+    total = sum(v[1] for v in prof.values())
+    for name, (launches, tot_ms) in prof.items():
+        kind, amt = work.get(name, ("bytes", 0))
+        avg = tot_ms / launches
+        rate = amt / (tot_ms / 1e3) if tot_ms > 0 else 0.0
+        ent = {"launches": launches, "avg_us": 1e3 * avg, "total_ms": tot_ms, "share": tot_ms / total}
+        if kind == "bytes":
+            ent.update({"achieved": rate / 1e9, "unit": "GB/s", "frac": rate / 1e9 / hbm})
+        else:
+            ent.update({"achieved": rate / 1e12, "unit": "TFLOP/s", "frac": rate / 1e12 / tc})
+        ent["algorithmic_per_launch"] = amt / launches
+        kernels[name] = ent
+    dom = max(kernels, key=lambda k: kernels[k]["share"])
+    kd = kernels[dom]
+    kind = work[dom][0]
+    roof = {"kernel": dom, "bound": "hbm" if kind == "bytes" else "tensor", "achieved": kd["achieved"],
+            "peak": hbm if kind == "bytes" else tc, "unit": kd["unit"], "frac": kd["frac"],
+            "traffic": None, "peak_source": pk["source"] + (" (sustained)" if kind != "bytes" else "")}
+    # whole-job roofline: bytes at HBM bandwidth + hashing flops at tensor peak
+    t_roof = sum(v[1] / (hbm * 1e9) for k, v in work.items() if v[0] == "bytes" and k in prof)
+    t_roof += sum(v[1] / (tc * 1e12) for k, v in work.items() if v[0] == "flops" and k in prof)
+    build_ms = sum(prof[k][1] for k in ("prepare_w", "center", "hash_keys_tc", "hash_keys_simt", "csr_build")
+                   if k in prof)
+    dec_ms = total - build_ms
+    x = 0.5 ** wl.K
+    closed = 1 - (1 - x) ** wl.L - wl.L * x * (1 - x) ** (wl.L - 1)
+    region = sum(max(0, wl.seq_len(t) - wl.window - min(s, wl.seq_len(t))) for t in range(steps)) * Q
+    return {
+        "kernels": kernels, "roofline": roof,
+        "pipeline_roofline": {"roofline_ms": 1e3 * t_roof, "measured_ms": total,
+                              "frac": (1e3 * t_roof) / total if total else None},
+        "build_ms": build_ms, "us_per_decode_step": 1e3 * dec_ms / steps,
+        "sampled_fraction": sampled_entries / region if region else None,
+        "closed_form_fraction": closed,
+    }
+
+
+def run_e2e(job, stream, args, world):
+    """Same job through the public API with host buffers: pinned host inputs copied in
+    and outputs copied back inside the timed region."""
+    import torch
+    h_keys = torch.empty(job.keys.shape, dtype=job.keys.dtype, pin_memory=True)
+    h_vals = torch.empty(job.values.shape, dtype=job.values.dtype, pin_memory=True)
+    h_W = torch.empty(job.W.shape, dtype=job.W.dtype, pin_memory=True)
+    h_q = torch.empty(job.queries.shape, dtype=job.queries.dtype, pin_memory=True)
+    h_out = torch.empty(job.outs.shape, dtype=job.outs.dtype, pin_memory=True)
+    h_keys.copy_(job.keys)
+    h_vals.copy_(job.values)
+    h_W.copy_(job.W)
+    h_q.copy_(job.queries)
+    d_keys = torch.empty_like(job.keys)
+    d_vals = torch.empty_like(job.values)
+    d_W = torch.empty_like(job.W)
+    d_q = torch.empty_like(job.queries)
+    torch.cuda.synchronize()
+
+    def one():
+        d_keys.copy_(h_keys, non_blocking=True)
+        d_vals.copy_(h_vals, non_blocking=True)
+        d_W.copy_(h_W, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
+        job.build(keys=d_keys, W=d_W)
+        job.decode_steps(keys=d_keys, values=d_vals, queries=d_q)
+        h_out.copy_(job.outs, non_blocking=True)
+
+    n = max(1, min(args.steps, 3))
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            one()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, True) / n
+    bi = sum(t.numel() * t.element_size() for t in (h_keys, h_vals, h_W, h_q))
+    bo = h_out.numel() * h_out.element_size()
+    del d_keys, d_vals, d_W, d_q
+    return {"value": job.queries_per_job * world / (ms / 1e3), "unit": "queries/s", "ms_per_step": ms,
+            "steps": n, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# ----------------------------------------------------------------------------------
+# CPU oracle timing (bounded sample of the same workload)
+# ----------------------------------------------------------------------------------
+
+def oracle_sample(wl, decode_steps: int = 4):
+    """Time the fp64 oracle on one KV head of the workload: its table build (all
+    tokens hashed) and `decode_steps` decode steps for each of its query heads; scale
+    to the whole job by unit counts. Returns (queries/s, seconds spent, description)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    import workloads as WL
+    cap, d = wl.capacity, wl.head_dim
+    k = WL.round_to(WL.keys_block(wl, 0, 0, 0, 0, cap), wl.dtype).double().numpy()
+    v = WL.round_to(WL.values_block(wl, 0, 0, 0, 0, cap), wl.dtype).double().numpy()
+    W = WL.projection(wl, 0).double().numpy()
+    t0 = time.perf_counter()
+    tab = O.HeadTables(k, W, wl.K, wl.L, wl.n_sink, wl.n_prefill, n_total=cap)
+    t_build = time.perf_counter() - t0
+    steps = list(range(min(decode_steps, wl.steps)))
+    nq = 0
+    t1 = time.perf_counter()
+    for s in steps:
+        q = WL.round_to(WL.query_block(wl, s, 0, 0), wl.dtype).double().numpy()
+        n = wl.seq_len(s)
+        for g in range(wl.group):
+            O.decode_head(q[g], k[:n], v[:n], tab, n, wl.window)
+            nq += 1
+    t_dec = time.perf_counter() - t1
+    U = wl.layers * wl.batch * wl.kv_heads
+    total_q = wl.steps * wl.layers * wl.batch * wl.q_heads
+    job_s = t_build * U + t_dec * (total_q / nq)
+    desc = (f"one KV head (layer 0, sequence 0, head 0): table build over {cap} tokens "
+            f"({t_build:.2f} s) + {len(steps)} decode steps x {wl.group} query heads ({t_dec:.2f} s); "
+            f"job time scaled by {U} heads and {total_q} queries")
+    return total_q / job_s, t_build + t_dec, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    import workloads as WL
+    wl = WL.WORKLOADS[args.workload]
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample(wl, decode_steps=1)
+    vals, secs = [], 0.0
+    t0 = time.perf_counter()
+    desc = ""
+    for _ in range(args.steps):
+        v, sec, desc = oracle_sample(wl, decode_steps=1)
+        vals.append(v)
+        secs += sec
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same recipe as the GPU arm)",
+        "config": {"workload": wl.name, "step": "bounded sample of the job on the CPU oracle"},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup(True)
+    line, job = run_ours(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import workloads as WL
+        v, sec, desc = oracle_sample(WL.WORKLOADS[args.workload], decode_steps=4)
+        line["cpu_baseline"] = {"value": v, "unit": "queries/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc, "seconds": sec}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

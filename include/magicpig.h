@@ -72,8 +72,9 @@ extern "C" {
 #define MP_DTYPE_BF16 1
 
 /* how the sampled set is found */
-#define MP_MATCH_AUTO 0 /* choose by bytes moved per query */
+#define MP_MATCH_AUTO 0 /* choose by bytes moved per query head (fewer wins) */
 #define MP_MATCH_CSR 1  /* bucketed tables: one id list per (KV head, table, code) */
+#define MP_MATCH_SCAN 2 /* stream bit-planes of every code, shared by the query heads of a KV head */
 
 typedef struct mp_config {
   int32_t layers;      /* independent attention layers handled by one call */
@@ -88,7 +89,7 @@ typedef struct mp_config {
   int32_t capacity;    /* maximum tokens per sequence (prefill + appended), <= 2^19 */
   int32_t dtype;       /* MP_DTYPE_BF16 or MP_DTYPE_F32 (keys, values, q) */
   int32_t w_per_layer; /* 1: W holds one matrix per layer; 0: one matrix shared by all layers */
-  int32_t match_mode;  /* MP_MATCH_AUTO or MP_MATCH_CSR */
+  int32_t match_mode;  /* MP_MATCH_AUTO, MP_MATCH_CSR or MP_MATCH_SCAN */
   int32_t threshold;   /* minimum colliding tables for a key to be sampled: 1 or 2 (pages: 2) */
   int32_t reserved[4]; /* must be zero */
 } mp_config;
@@ -100,17 +101,23 @@ typedef struct mp_tables_layout {
   uint64_t total_bytes;
   uint64_t header;       /* 256 B: magic, prefill length, appended length, status word */
   uint64_t center;       /* float [U][d]: mean key of tokens [n_sink, n_prefill) */
-  uint64_t beta;         /* float [U][KLp]: W^T · center */
+  uint64_t beta;         /* float [U][TC]: W^T · center, tensor-core column order */
   uint64_t wt_f32;       /* float [layers or 1][KLp][d]: W transposed, zero-padded */
-  uint64_t wt_bf16;      /* bf16  [layers or 1][KLp][d] (bf16 configs only, else 0) */
+  uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: W transposed in tensor-core column order
+                            (bf16 configs only, else 0) */
   uint64_t center_parts; /* float [U][parts][d]: partial sums while building */
   uint64_t codes;        /* uint16 [U][L][capacity]: code of every hashed token, table-major */
-  uint64_t csr_offsets;  /* uint32 [U][L][NB+1]: bucket starts in csr_ids, per table */
-  uint64_t csr_ids;      /* uint32 [U][L][capacity]: token ids of [n_sink, n_prefill) by bucket, ascending */
-  int32_t kl_padded;
-  int32_t n_buckets;
+  uint64_t csr_offsets;  /* uint32 [U][L][NB+1]: bucket starts in csr_ids, per table (CSR mode, else 0) */
+  uint64_t csr_ids;      /* uint32 [U][L][capacity]: token ids of [n_sink, n_prefill) by bucket, ascending
+                            (CSR mode, else 0) */
+  uint64_t planes;       /* uint32 [U][L][K][CW]: bit-planes, word w bit i = bit b of the code of token
+                            32w+i (scan mode, else 0); CW = capacity/32 rounded up to a multiple of 4 */
+  int32_t kl_padded;     /* KLp */
+  int32_t n_buckets;     /* NB */
   int32_t parts;
-  int32_t reserved;
+  int32_t tc_cols;       /* TC: 256-column tiles, each holding floor(256/K) whole tables */
+  int32_t match_mode;    /* the mode in use: MP_MATCH_CSR or MP_MATCH_SCAN (AUTO resolved) */
+  int32_t cap_words;     /* CW */
 } mp_tables_layout;
 
 /* Byte offsets in the decode scratch buffer. Q = layers·batch·q_heads. */
@@ -123,6 +130,7 @@ typedef struct mp_decode_layout {
                             (bit 31 set on exact tokens) */
   uint64_t partials;     /* float [Q][splits_max][d+2]: split-K partial (m, l, acc[d]) */
   uint64_t counters;     /* uint32 [Q]: split-K completion counters */
+  uint64_t sample_bits;  /* uint32 [Q][CW]: sampled-token bitmaps (scan mode, else 0) */
   int32_t splits_max;
   int32_t reserved;
 } mp_decode_layout;

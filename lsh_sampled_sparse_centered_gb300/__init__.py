@@ -32,6 +32,7 @@ MP_DTYPE_F32 = 0
 MP_DTYPE_BF16 = 1
 MP_MATCH_AUTO = 0
 MP_MATCH_CSR = 1
+MP_MATCH_SCAN = 2
 
 EXACT_FLAG = 0x80000000
 
@@ -51,13 +52,14 @@ class mp_config(ctypes.Structure):
 class mp_tables_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "total_bytes", "header", "center", "beta", "wt_f32", "wt_bf16", "center_parts", "codes",
-        "csr_offsets", "csr_ids")] + [(n, ctypes.c_int32) for n in (
-        "kl_padded", "n_buckets", "parts", "reserved")]
+        "csr_offsets", "csr_ids", "planes")] + [(n, ctypes.c_int32) for n in (
+        "kl_padded", "n_buckets", "parts", "tc_cols", "match_mode", "cap_words")]
 
 
 class mp_decode_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
-        "total_bytes", "q_codes", "list_len", "sample_count", "lists", "partials", "counters")] + [
+        "total_bytes", "q_codes", "list_len", "sample_count", "lists", "partials", "counters",
+        "sample_bits")] + [
         (n, ctypes.c_int32) for n in ("splits_max", "reserved")]
 
 

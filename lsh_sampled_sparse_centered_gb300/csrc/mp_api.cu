@@ -19,7 +19,8 @@ static int check_config(const mp_config* c) {
   if (c->K < 0 || c->L < 1 || c->n_sink < 0 || c->window < 0 || c->capacity < 1) return MP_ERR_INVALID_ARG;
   if (c->dtype != MP_DTYPE_F32 && c->dtype != MP_DTYPE_BF16) return MP_ERR_INVALID_ARG;
   if (c->w_per_layer != 0 && c->w_per_layer != 1) return MP_ERR_INVALID_ARG;
-  if (c->match_mode != MP_MATCH_AUTO && c->match_mode != MP_MATCH_CSR) return MP_ERR_INVALID_ARG;
+  if (c->match_mode != MP_MATCH_AUTO && c->match_mode != MP_MATCH_CSR && c->match_mode != MP_MATCH_SCAN)
+    return MP_ERR_INVALID_ARG;
   if (c->threshold < 1 || c->threshold > c->L) return MP_ERR_INVALID_ARG;
   for (int i = 0; i < 4; ++i)
     if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
@@ -30,6 +31,18 @@ static int check_config(const mp_config* c) {
   const int64_t q = int64_t(c->layers) * c->batch * c->q_heads;
   if (q > (1 << 30)) return MP_ERR_UNSUPPORTED;
   return MP_OK;
+}
+
+// AUTO: the mode that moves fewer bytes per query head and decode step.
+//   CSR : L buckets of ~m/2^K ids (4 B) + offsets and code (10 B) per table
+//   SCAN: m tokens x L tables x K bits, read once for the G query heads of a KV head
+static int resolve_match(const mp_config* c) {
+  if (c->match_mode != MP_MATCH_AUTO) return c->match_mode;
+  const double m = std::max(1, c->capacity - c->n_sink - c->window);
+  const double G = double(c->q_heads / c->kv_heads);
+  const double csr = c->L * (m / std::ldexp(1.0, c->K)) * 4.0 + c->L * 10.0;
+  const double scan = m * c->L * c->K / 8.0 / G;
+  return scan < csr ? MP_MATCH_SCAN : MP_MATCH_CSR;
 }
 
 static Geometry geometry(const mp_config* c) {
@@ -54,6 +67,11 @@ static Geometry geometry(const mp_config* c) {
   g.klp = int(align256(uint64_t(g.kl)));
   if (g.klp == 0) g.klp = 256;
   g.nb = 1 << c->K;
+  g.tpt = c->K > 0 ? 256 / c->K : 0;
+  g.nt = c->K > 0 ? (c->L + g.tpt - 1) / g.tpt : 0;
+  g.kltc = g.nt * 256;
+  g.match = resolve_match(c);
+  g.cw = (((c->capacity + 31) / 32) + 3) & ~3;
   g.parts = 32;
   g.n_w = c->w_per_layer ? c->layers : 1;
   return g;
@@ -68,25 +86,33 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
   o->center = off;
   off = align256(off + U * d * 4);
   o->beta = off;
-  off = align256(off + U * uint64_t(g.klp) * 4);
+  off = align256(off + U * uint64_t(g.kltc) * 4);
   o->wt_f32 = off;
   off = align256(off + uint64_t(g.n_w) * g.klp * d * 4);
   if (g.dtype == MP_DTYPE_BF16) {
     o->wt_bf16 = off;
-    off = align256(off + uint64_t(g.n_w) * g.klp * d * 2);
+    off = align256(off + uint64_t(g.n_w) * g.kltc * d * 2);
   }
   o->center_parts = off;
   off = align256(off + U * uint64_t(g.parts) * d * 4);
   o->codes = off;
   off = align256(off + U * L * cap * 2);
-  o->csr_offsets = off;
-  off = align256(off + U * L * (uint64_t(g.nb) + 1) * 4);
-  o->csr_ids = off;
-  off = align256(off + U * L * cap * 4);
+  if (g.match == MP_MATCH_CSR) {
+    o->csr_offsets = off;
+    off = align256(off + U * L * (uint64_t(g.nb) + 1) * 4);
+    o->csr_ids = off;
+    off = align256(off + U * L * cap * 4);
+  } else {
+    o->planes = off;
+    off = align256(off + U * L * uint64_t(g.K) * g.cw * 4);
+  }
   o->total_bytes = off;
   o->kl_padded = g.klp;
   o->n_buckets = g.nb;
   o->parts = g.parts;
+  o->tc_cols = g.kltc;
+  o->match_mode = g.match;
+  o->cap_words = g.cw;
 }
 
 static void decode_layout(const Geometry& g, mp_decode_layout* o) {
@@ -105,6 +131,10 @@ static void decode_layout(const Geometry& g, mp_decode_layout* o) {
   off = align256(off + Q * kSplitsMax * uint64_t(g.d + 2) * 4);
   o->counters = off;
   off = align256(off + Q * 4);
+  if (g.match == MP_MATCH_SCAN) {
+    o->sample_bits = off;
+    off = align256(off + Q * uint64_t(g.cw) * 4);
+  }
   o->total_bytes = off;
   o->splits_max = kSplitsMax;
 }
@@ -121,8 +151,9 @@ static TablesPtrs tables_ptrs(const Geometry& g, void* base) {
   t.wt16 = l.wt_bf16 ? reinterpret_cast<__nv_bfloat16*>(b + l.wt_bf16) : nullptr;
   t.cparts = reinterpret_cast<float*>(b + l.center_parts);
   t.codes = reinterpret_cast<uint16_t*>(b + l.codes);
-  t.off = reinterpret_cast<uint32_t*>(b + l.csr_offsets);
-  t.ids = reinterpret_cast<uint32_t*>(b + l.csr_ids);
+  t.off = l.csr_offsets ? reinterpret_cast<uint32_t*>(b + l.csr_offsets) : nullptr;
+  t.ids = l.csr_ids ? reinterpret_cast<uint32_t*>(b + l.csr_ids) : nullptr;
+  t.planes = l.planes ? reinterpret_cast<uint32_t*>(b + l.planes) : nullptr;
   return t;
 }
 
@@ -137,6 +168,7 @@ static DecodePtrs decode_ptrs(const Geometry& g, void* base) {
   p.lists = reinterpret_cast<uint32_t*>(b + l.lists);
   p.partials = reinterpret_cast<float*>(b + l.partials);
   p.counters = reinterpret_cast<uint32_t*>(b + l.counters);
+  p.sbits = l.sample_bits ? reinterpret_cast<uint32_t*>(b + l.sample_bits) : nullptr;
   return p;
 }
 
@@ -191,11 +223,12 @@ static int choose_splits(const Geometry& g, int n) {
 // ---- optional per-launch event timing ----
 enum KernelId {
   K_PREPARE_W, K_CENTER, K_HASH_KEYS_SIMT, K_HASH_KEYS_TC, K_CSR_BUILD, K_HASH_APPEND, K_MARK_APPENDED,
-  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_COUNT
+  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_PLANES_BUILD, K_PLANES_APPEND, K_SCAN, K_COMPACT, K_COUNT
 };
 static const char* kKernelNames[K_COUNT] = {"prepare_w", "center", "hash_keys_simt", "hash_keys_tc",
                                             "csr_build", "hash_append", "mark_appended", "hash_query",
-                                            "match_csr", "attend"};
+                                            "match_csr", "attend", "planes_build", "planes_append",
+                                            "scan", "compact"};
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
@@ -327,9 +360,12 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
     ProfScope ps(st, K_HASH_KEYS_SIMT);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
   }
-  {
+  if (g.match == MP_MATCH_CSR) {
     ProfScope ps(st, K_CSR_BUILD);
     if (launch_csr_build(g, n_prefill, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
+    ProfScope ps(st, K_PLANES_BUILD);
+    if (launch_planes_build(g, n_prefill, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
@@ -369,6 +405,10 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   {
     ProfScope ps(st, K_HASH_APPEND);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  if (g.match == MP_MATCH_SCAN) {
+    ProfScope ps(st, K_PLANES_APPEND);
+    if (launch_planes_append(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   {
     ProfScope ps(st, K_MARK_APPENDED);
@@ -418,9 +458,16 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   // 2. sampled set (Algorithm 1 'Query') + exact tokens
-  {
+  if (g.match == MP_MATCH_CSR) {
     ProfScope ps(st, K_MATCH_CSR);
     if (launch_match_csr(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
+    {
+      ProfScope ps(st, K_SCAN);
+      if (launch_scan(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+    }
+    ProfScope ps(st, K_COMPACT);
+    if (launch_compact(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   // 3. split-K importance-weighted attention with fused combine
   const int splits = choose_splits(g, n);

@@ -4,6 +4,7 @@
 // MagicPIG (arXiv 2410.16179v2): Algorithm 1, Eq. 9-11, §4.4 "On-device cache".
 #include <math_constants.h>
 
+#include "mp_compact.cuh"
 #include "mp_internal.h"
 
 namespace mp {
@@ -32,8 +33,6 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
   uint32_t* seen1 = sm;
   uint32_t* seen2 = sm + nwords;
   uint16_t* qc = reinterpret_cast<uint16_t*>(sm + 2 * nwords);
-  __shared__ uint32_t wsum[8];
-  __shared__ int s_total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   const bool built = hdr->magic == kMagic;
@@ -83,61 +82,8 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
   __syncthreads();
 
   // compaction of [lo, hi)
-  const uint32_t* sel = threshold >= 2 ? seen2 : seen1;
-  const int w0 = lo >> 5;
-  const int nw = nwords - w0;
-  const int per = (nw + blockDim.x - 1) / blockDim.x;
-  const int my0 = w0 + threadIdx.x * per, my1 = min(nwords, my0 + per);
-  auto word_at = [&](int wi) -> uint32_t {
-    uint32_t v = sel[wi];
-    const int base = wi << 5;
-    if (base < lo) v &= ~((1u << (lo - base)) - 1u);        // lo - base in 1..31
-    if (base + 32 > hi) v &= (hi - base >= 32) ? 0xffffffffu : ((1u << (hi - base)) - 1u);
-    return v;
-  };
-  int local = 0;
-  for (int wi = my0; wi < my1; ++wi) local += __popc(word_at(wi));
-  int x = local;
-#pragma unroll
-  for (int k = 1; k < 32; k <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, k);
-    if (lane >= k) x += y;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < 8; ++i) {
-      const int v = wsum[i];
-      wsum[i] = run;
-      run += v;
-    }
-    s_total = run;
-  }
-  __syncthreads();
-  int pos = wsum[warp] + x - local;
-  uint32_t* lst = lists + int64_t(qh) * cap;
-  if (built) {
-    for (int wi = my0; wi < my1; ++wi) {
-      uint32_t v = word_at(wi);
-      while (v) {
-        const int b = __ffs(v) - 1;
-        v &= v - 1;
-        lst[pos++] = uint32_t((wi << 5) + b);
-      }
-    }
-  }
-  const int ns = built ? s_total : 0;
-  // exact tokens: [0, lo) then [hi, n)
-  const int nexact = lo + (n - hi);
-  for (int i = threadIdx.x; i < nexact; i += blockDim.x) {
-    const int tok = i < lo ? i : hi + (i - lo);
-    lst[ns + i] = uint32_t(tok) | kExactFlag;
-  }
-  if (threadIdx.x == 0) {
-    sample_count[qh] = ns;
-    list_len[qh] = ns + nexact;
-  }
+  write_list(threshold >= 2 ? seen2 : seen1, built, lo, hi, n, lists + int64_t(qh) * cap, &sample_count[qh],
+             &list_len[qh]);
 }
 
 cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp,
@@ -204,11 +150,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Returns false if the phase did not complete within the iteration limit.
+// Returns false if the phase did not complete within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (int i = 0; i < (1 << 22); ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

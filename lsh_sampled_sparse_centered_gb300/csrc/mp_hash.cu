@@ -10,11 +10,14 @@
 namespace mp {
 
 // ---------------------------------------------------------------------------------
-// W [n_w][d][K*L] fp32  ->  wt32 [n_w][KLp][d] fp32, wt16 [n_w][KLp][d] bf16
+// W [n_w][d][K*L] fp32  ->  wt32 [n_w][KLp][d] fp32 (column j = t*K + b, zero padded)
+//                       ->  wt16 [n_w][TC][d] bf16 in tensor-core column order: tile
+//                           n holds tables n*tpt .. n*tpt+tpt-1, column n*256 + i*K + b
+//                           is bit b of the tile's i-th table; the rest is zero.
 // ---------------------------------------------------------------------------------
 __global__ void k_prepare_w(const float* __restrict__ W, float* __restrict__ wt32,
-                            __nv_bfloat16* __restrict__ wt16, int d, int kl, int klp,
-                            uint32_t* status) {
+                            __nv_bfloat16* __restrict__ wt16, int d, int K, int L, int kl, int klp, int tpt,
+                            int kltc, uint32_t* status) {
   // tile transpose: 32 columns x 32 d-rows per block
   __shared__ float tile[32][33];
   const int m = blockIdx.z;
@@ -25,26 +28,33 @@ __global__ void k_prepare_w(const float* __restrict__ W, float* __restrict__ wt3
     tile[r][tx] = (dd < d && j < kl) ? W[(int64_t(m) * d + dd) * kl + j] : 0.f;
   }
   __syncthreads();
-  bool inexact = false;
   for (int r = ty; r < 32; r += 8) {
     const int j = j0 + r, dd = d0 + tx;
-    if (j < klp && dd < d) {
-      const float v = tile[tx][r];
-      const int64_t o = (int64_t(m) * klp + j) * d + dd;
-      wt32[o] = v;
-      if (wt16) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        wt16[o] = b;
-        inexact |= (__bfloat162float(b) != v);
-      }
-    }
+    if (j < klp && dd < d) wt32[(int64_t(m) * klp + j) * d + dd] = tile[tx][r];
+  }
+  if (!wt16) return;
+  // tensor-core order: this block also writes TC columns jc in [j0, j0 + 32)
+  bool inexact = false;
+  for (int r = ty; r < 32; r += 8) {
+    const int jc = j0 + r, dd = d0 + tx;
+    if (jc >= kltc || dd >= d) continue;
+    const int n = jc >> 8, within = jc & 255;
+    const int i = within / K, b = within - i * K;
+    const int t = n * tpt + i;
+    float v = 0.f;
+    if (i < tpt && t < L) v = W[(int64_t(m) * d + dd) * kl + t * K + b];
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    wt16[(int64_t(m) * kltc + jc) * d + dd] = h;
+    inexact |= (__bfloat162float(h) != v);
   }
   if (inexact) atomicOr(status, MP_STATUS_W_NOT_BF16);
 }
 
 cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st) {
-  dim3 grid((g.klp + 31) / 32, (g.d + 31) / 32, g.n_w), block(32, 8);
-  k_prepare_w<<<grid, block, 0, st>>>(W, t.wt32, t.wt16, g.d, g.kl, g.klp, &t.hdr->status);
+  const int cols = max(g.klp, g.kltc);
+  dim3 grid((cols + 31) / 32, (g.d + 31) / 32, g.n_w), block(32, 8);
+  k_prepare_w<<<grid, block, 0, st>>>(W, t.wt32, t.wt16, g.d, g.K, g.L, g.kl, g.klp, g.tpt, g.kltc,
+                                      &t.hdr->status);
   return cudaGetLastError();
 }
 
@@ -74,9 +84,9 @@ __global__ void k_center_parts(const T* __restrict__ keys, float* __restrict__ c
 }
 
 __global__ void k_center_final(const float* __restrict__ cparts, float* __restrict__ center,
-                               float* __restrict__ beta, const float* __restrict__ wt32, int d, int klp,
-                               int parts, int count, int units_per_w, int64_t w_stride, DevHeader* hdr,
-                               int n_prefill) {
+                               float* __restrict__ beta, const __nv_bfloat16* __restrict__ wt16, int d,
+                               int kltc, int parts, int count, int units_per_w, int64_t w_stride,
+                               DevHeader* hdr, int n_prefill) {
   extern __shared__ float c[];  // [d]
   const int u = blockIdx.x;
   for (int dim = threadIdx.x; dim < d; dim += blockDim.x) {
@@ -87,12 +97,15 @@ __global__ void k_center_final(const float* __restrict__ cparts, float* __restri
     center[int64_t(u) * d + dim] = v;
   }
   __syncthreads();
-  const float* w = wt32 + int64_t(u / units_per_w) * w_stride;
-  for (int j = threadIdx.x; j < klp; j += blockDim.x) {
-    const float* row = w + int64_t(j) * d;
-    float s = 0.f;
-    for (int dim = 0; dim < d; ++dim) s = fmaf(row[dim], c[dim], s);
-    beta[int64_t(u) * klp + j] = s;
+  // beta = W^T c in tensor-core column order (used by the tensor-core hash)
+  if (wt16) {
+    const __nv_bfloat16* w = wt16 + int64_t(u / units_per_w) * w_stride;
+    for (int j = threadIdx.x; j < kltc; j += blockDim.x) {
+      const __nv_bfloat16* row = w + int64_t(j) * d;
+      float s = 0.f;
+      for (int dim = 0; dim < d; ++dim) s = fmaf(__bfloat162float(row[dim]), c[dim], s);
+      beta[int64_t(u) * kltc + j] = s;
+    }
   }
   if (u == 0 && threadIdx.x == 0) {
     hdr->n_prefill = n_prefill;
@@ -115,9 +128,9 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
         static_cast<const float*>(keys), t.cparts, g.d, g.cap, lo, hi, g.parts);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
-  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.wt32, g.d,
-                                                          g.klp, g.parts, hi - lo, g.batch * g.kvh,
+  const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
+  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.wt16, g.d,
+                                                          g.kltc, g.parts, hi - lo, g.batch * g.kvh,
                                                           w_stride, t.hdr, n_prefill);
   return cudaGetLastError();
 }

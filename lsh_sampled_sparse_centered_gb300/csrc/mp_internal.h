@@ -34,6 +34,11 @@ struct Geometry {
   int queries;  // layers * batch * q_heads
   int kl, klp;  // K*L and K*L rounded up to 256
   int nb;       // 2^K
+  int tpt;      // tables per 256-column tensor-core tile: floor(256 / K)
+  int nt;       // tensor-core column tiles: ceil(L / tpt)
+  int kltc;     // nt * 256
+  int match;    // MP_MATCH_CSR or MP_MATCH_SCAN (AUTO resolved)
+  int cw;       // bit-plane words per table row: ceil(cap/32) rounded up to a multiple of 4
   int parts;    // partial sums per unit for the center
   int n_w;      // number of W matrices
 };
@@ -48,6 +53,7 @@ struct TablesPtrs {
   uint16_t* codes;
   uint32_t* off;
   uint32_t* ids;
+  uint32_t* planes;
 };
 
 struct DecodePtrs {
@@ -57,6 +63,7 @@ struct DecodePtrs {
   uint32_t* lists;
   float* partials;
   uint32_t* counters;
+  uint32_t* sbits;
 };
 
 // Rows to hash: row r (0-based) of group g lives at
@@ -87,6 +94,10 @@ cudaError_t launch_csr_build(const Geometry& g, int n_prefill, const TablesPtrs&
 cudaError_t launch_mark_appended(const Geometry& g, int pos, const TablesPtrs& t, cudaStream_t st);
 cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp,
                              cudaStream_t st);
+cudaError_t launch_planes_build(const Geometry& g, int n_prefill, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_planes_append(const Geometry& g, int pos, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_scan(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp, cudaStream_t st);
+cudaError_t launch_compact(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp, cudaStream_t st);
 cudaError_t launch_attend(const Geometry& g, int n, int splits, const TablesPtrs& t, const void* keys,
                           const void* values, const void* q, float* out, const DecodePtrs& dp,
                           cudaStream_t st);
@@ -94,6 +105,14 @@ cudaError_t launch_attend(const Geometry& g, int n, int splits, const TablesPtrs
 int device_sm_count();
 
 #ifdef __CUDACC__
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Limit of every spin-wait on an mbarrier: the wait gives up after this long.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 #endif

@@ -10,20 +10,20 @@ import oracle as O
 import workloads as WL
 
 
-def config_for(mp, wl: WL.Workload, threshold: int = 2):
+def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0):
     return mp.make_config(layers=wl.layers, batch=wl.batch, kv_heads=wl.kv_heads, q_heads=wl.q_heads,
                           head_dim=wl.head_dim, K=wl.K, L=wl.L, n_sink=wl.n_sink, window=wl.window,
                           capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer,
-                          threshold=threshold)
+                          threshold=threshold, match_mode=match_mode)
 
 
 class GpuRun:
     """Buffers and calls for one workload on one device."""
 
-    def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2):
+    def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2, match_mode: int = 0):
         self.mp, self.wl, self.dev = mp, wl, torch.device(device)
         self.threshold = threshold
-        self.cfg = config_for(mp, wl, threshold)
+        self.cfg = config_for(mp, wl, threshold, match_mode)
         self.tl = mp.mp_tables_layout_get(self.cfg)
         self.dl = mp.mp_decode_layout_get(self.cfg)
         self.tables = torch.empty(self.tl.total_bytes, dtype=torch.uint8, device=self.dev)
@@ -80,6 +80,13 @@ class GpuRun:
         ids = self.tables[i0: i0 + tables * wl.capacity * 4].view(torch.int32)
         return (off.cpu().numpy().astype(np.int64).reshape(tables, nb + 1),
                 ids.cpu().numpy().astype(np.int64).reshape(tables, wl.capacity))
+
+    def unit_planes(self, u: int, tables: int) -> np.ndarray:
+        """Bit-planes of unit u for the first `tables` tables, [tables, K, CW] as int64."""
+        wl, cw = self.wl, self.tl.cap_words
+        o = self.tl.planes + u * wl.L * wl.K * cw * 4
+        v = self.tables[o: o + tables * wl.K * cw * 4].view(torch.int32)
+        return (v.cpu().numpy().astype(np.int64) & 0xFFFFFFFF).reshape(tables, wl.K, cw)
 
     def center(self) -> np.ndarray:
         wl = self.wl
@@ -167,11 +174,19 @@ def host_unit(tensors, wl, layer, b, h, n):
     return k, v
 
 
+def check_planes(planes: np.ndarray, codes: np.ndarray, n: int, K: int) -> None:
+    """Bit-planes [K, CW] of one table against codes [n] of tokens [0, n)."""
+    for b in range(K):
+        bits = (planes[b][:, None] >> np.arange(32)[None, :]) & 1
+        np.testing.assert_array_equal(bits.reshape(-1)[:n], (codes[:n] >> b) & 1)
+
+
 def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshold: int = 2,
-                   units=None, qheads=None, steps=None, check_csr_tables: int = 8, tol: float = 2e-3) -> dict:
+                   units=None, qheads=None, steps=None, check_csr_tables: int = 8, tol: float = 2e-3,
+                   match_mode: int = 0) -> dict:
     """Build, append and decode `wl` through the C ABI and compare every stage with the
     oracle on the chosen units / query heads / steps. Returns counters for reporting."""
-    run = GpuRun(mp, wl, tensors, device, threshold)
+    run = GpuRun(mp, wl, tensors, device, threshold, match_mode)
     run.build()
     torch.cuda.synchronize()
     assert run.status() == 0, hex(run.status())
@@ -180,7 +195,7 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
     units = all_units if units is None else units
     steps = list(range(wl.steps)) if steps is None else steps
     rep = {"code_bits_tie": 0, "codes_differ": 0, "q_codes_differ": 0, "heads": 0, "max_rel_l2": 0.0,
-           "sampled": 0, "region": 0, "S_differ_oracle_codes": 0}
+           "sampled": 0, "region": 0, "S_differ_oracle_codes": 0, "match_mode": int(run.tl.match_mode)}
     n_tot = wl.capacity
     oracle_tabs = {}
     centers = run.center()
@@ -199,10 +214,15 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
         np.testing.assert_allclose(centers[u], tab.center, rtol=1e-5, atol=1e-5)
         lo = min(wl.n_sink, n0)
         nt = min(wl.L, check_csr_tables)
-        off, ids = run.unit_csr(u, nt)
         gc = run.unit_codes(u, n0)
-        for t in range(nt):
-            check_csr(off[t], ids[t], gc[:, t], lo, n0, run.tl.n_buckets)
+        if run.tl.match_mode == mp.MP_MATCH_CSR:
+            off, ids = run.unit_csr(u, nt)
+            for t in range(nt):
+                check_csr(off[t], ids[t], gc[:, t], lo, n0, run.tl.n_buckets)
+        else:
+            pl = run.unit_planes(u, nt)
+            for t in range(nt):
+                check_planes(pl[t], gc[:, t], n0, wl.K)
     last = max(steps) if steps else -1
     for step in range(last + 1):
         n = wl.seq_len(step)
@@ -220,6 +240,10 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
             u = unit_index(wl, l, b, h)
             tab = oracle_tabs[u]
             kc = run.unit_codes(u, n)
+            if wl.append and run.tl.match_mode == mp.MP_MATCH_SCAN:
+                pl = run.unit_planes(u, min(wl.L, check_csr_tables))
+                for t in range(pl.shape[0]):
+                    check_planes(pl[t], kc[:, t], n, wl.K)
             if wl.append:
                 tiec = tie_codes(tab.ties[n - 1: n], wl.K, wl.L)
                 cmp = compare_codes(kc[n - 1: n], tab.codes[n - 1: n], tiec)

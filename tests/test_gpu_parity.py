@@ -24,7 +24,7 @@ def mp():
 
 
 def _report(name, rep):
-    print(f"\n[{name}] heads={rep['heads']} max_rel_l2={rep['max_rel_l2']:.2e} "
+    print(f"\n[{name}] mode={'csr' if rep['match_mode'] == 1 else 'scan'} heads={rep['heads']} max_rel_l2={rep['max_rel_l2']:.2e} "
           f"sampled_frac={rep['sampled'] / max(1, rep['region']):.4f} codes_differ(near-tie)={rep['codes_differ']} "
           f"q_codes_differ(near-tie)={rep['q_codes_differ']} S_differ_vs_oracle_codes={rep['S_differ_oracle_codes']}")
 
@@ -119,3 +119,62 @@ def test_status_flags(mp):
     assert run.status() == 0
     run.decode(0, 350)
     assert run.status() == mp.MP_STATUS_APPEND_GAP
+
+
+@pytest.mark.parametrize("path", ["simt", "tc"])
+def test_both_key_hash_paths_match_the_oracle(mp, path, monkeypatch):
+    """Prefill keys are hashed on tensor cores (default) or on CUDA cores
+    (MP_HASH_PATH=simt); both must give the oracle's codes except near ties."""
+    monkeypatch.setenv("MP_HASH_PATH", path)
+    wl = WL.Workload("paths", layers=2, batch=1, kv_heads=2, q_heads=4, head_dim=128, n_prefill=4099, steps=1,
+                     append=False, K=10, L=50, dtype="bf16", seed=41, w_per_layer=True)
+    rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=50)
+    _report(f"hash path {path}", rep)
+
+
+@pytest.mark.parametrize("K,L,d", [(9, 120, 128), (12, 40, 128), (7, 33, 64), (1, 5, 64)])
+def test_tensor_core_hash_tile_layouts(mp, K, L, d):
+    """Tables per 256-column tile = floor(256/K): K values that leave padding columns,
+    L not a multiple of it, both head dims."""
+    wl = WL.Workload(f"tc-{K}-{L}-{d}", layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=d, n_prefill=700,
+                     steps=1, append=False, K=K, L=L, dtype="bf16", seed=K * 100 + L)
+    rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=L)
+    _report(f"tc K={K} L={L} d={d}", rep)
+
+
+# ----------------------------------------------------------------------------------
+# full-size workloads, same ABI calls as the benchmark; the oracle checks sampled
+# KV heads (all their query heads) at the first and last decode steps
+# ----------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg,units,steps", [
+    (2, [(0, 0, 0), (31, 0, 7)], [0, 63]),
+    (3, [(0, 0, 0), (0, 15, 39)], [0, 31]),
+    (4, [(0, 0, 0), (0, 3, 7)], [0, 63]),
+])
+def test_full_size_workloads_sampled(mp, cfg, units, steps):
+    wl = WL.WORKLOADS[cfg]
+    t = WL.generate(wl, device="cuda")
+    torch.cuda.synchronize()
+    rep = check_workload(mp, wl, t, units=units, steps=steps, check_csr_tables=6)
+    _report(f"cfg{cfg} full size (sampled)", rep)
+    assert rep["heads"] == len(units) * wl.group * len(steps)
+    del t
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("wl", [
+    WL.WORKLOADS[1].replace(kv_heads=4, q_heads=16, n_prefill=6000),
+    RAGGED,
+    WL.Workload("scan-mha-t1", layers=1, batch=2, kv_heads=3, q_heads=3, head_dim=64, n_prefill=2222, steps=3,
+                append=True, K=5, L=17, dtype="f32", seed=77, w_bf16=False),
+    WL.Workload("scan-g16", layers=1, batch=1, kv_heads=1, q_heads=16, head_dim=128, n_prefill=3000, steps=1,
+                append=False, K=4, L=24, dtype="bf16", seed=78),
+], ids=["cfg1-like", "ragged", "mha-f32", "group16"])
+def test_scan_match_mode(mp, wl):
+    """Bit-plane streaming match, forced (and chosen by AUTO for small K / large groups)."""
+    steps = [0, 15, 16, 17, 39] if wl is RAGGED else None
+    rep = check_workload(mp, wl, WL.generate(wl), match_mode=mp.MP_MATCH_SCAN, steps=steps,
+                         check_csr_tables=wl.L)
+    _report(f"scan {wl.name}", rep)
+    assert rep["match_mode"] == mp.MP_MATCH_SCAN
