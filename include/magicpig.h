@@ -154,7 +154,7 @@ MP_API int mp_decode_layout_get(const mp_config* cfg, mp_decode_layout* out);
  * and bucket the ids of tokens [n_sink, n_prefill) per (head, table, code) —
  * the hash tables HT of Algorithm 1.
  *   keys    : device, layout above; rows [0, n_prefill) are read.
- *   W       : device float32, [layers or 1][d][K·L] per config.w_per_layer.
+ *   W       : device float32, [layers or 1][d][K·L] per config.w_per_layer (may be NULL when K = 0).
  *   tables  : device, mp_tables_layout_get(cfg).total_bytes.
  * 1 <= n_prefill <= capacity, else MP_ERR_CAPACITY. Resets the status word. */
 MP_API int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill,

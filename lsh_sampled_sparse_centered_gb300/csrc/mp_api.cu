@@ -315,7 +315,8 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
                     void* tables, void* stream) {
   int rc = check_config(cfg);
   if (rc != MP_OK) return rc;
-  if (!keys || !W || !tables) return MP_ERR_INVALID_ARG;
+  // W may be null only when it has no columns (K = 0)
+  if (!keys || !tables || (!W && cfg->K > 0)) return MP_ERR_INVALID_ARG;
   if (!aligned16(keys) || !aligned16(W) || (reinterpret_cast<uintptr_t>(tables) & 255u))
     return MP_ERR_INVALID_ARG;
   if (n_prefill < 1 || n_prefill > cfg->capacity) return MP_ERR_CAPACITY;
