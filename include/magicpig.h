@@ -182,6 +182,29 @@ MP_API int mp_decode_attention(const mp_config* cfg, void* tables, const void* k
                         const void* values, int32_t n, const void* q, float* out,
                         void* scratch, size_t scratch_bytes, void* stream);
 
+/* Size of the scratch array built into the library for mp_decode_attention_static. */
+#define MP_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* The decode step of mp_decode_attention for callers that cannot allocate device
+ * memory for its scratch buffer: for example a plugin whose host application owns
+ * all device memory, a server that reserved its whole memory budget up front, or a
+ * latency-critical loop that must not call cudaMalloc because it can block on the
+ * device. No counterpart on the pages: it is a deployment variant of the same call.
+ * Same arguments and results as mp_decode_attention, minus scratch and scratch_bytes.
+ * The scratch lives in a fixed device array of MP_STATIC_SCRATCH_BYTES (32 MiB)
+ * compiled into the library and held by every GPU that loads it until the process
+ * exits. Calls whose mp_decode_layout_get(cfg).total_bytes exceeds that size are
+ * rejected with MP_ERR_SCRATCH before anything is enqueued. The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture. Allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine). All calls share the array
+ * and it keeps the last call's contents; the counters that must start at zero are
+ * reset on the device by every call. Calls whose kernels overlap on the GPU race on
+ * the shared array: order them on one stream (or by events). */
+MP_API int mp_decode_attention_static(const mp_config* cfg, void* tables, const void* keys,
+                                      const void* values, int32_t n, const void* q, float* out,
+                                      void* stream);
+
 /* Copy the device status word to *status (synchronises `stream`). */
 MP_API int mp_get_status(const void* tables, uint32_t* status, void* stream);
 

@@ -80,6 +80,7 @@ _SIGS = {
     "mp_build_tables": (ctypes.c_int, [_CFG, _P, _I, _P, _P, _P]),
     "mp_append": (ctypes.c_int, [_CFG, _P, _P, _I, _P]),
     "mp_decode_attention": (ctypes.c_int, [_CFG, _P, _P, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mp_decode_attention_static": (ctypes.c_int, [_CFG, _P, _P, _P, _I, _P, _P, _P]),
     "mp_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "mp_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "mp_profile_read": (ctypes.c_int, [ctypes.POINTER(mp_kernel_time), ctypes.c_int32,
@@ -172,6 +173,15 @@ def mp_decode_attention(cfg: mp_config, tables, keys, values, n: int, q, out, sc
     return _check("mp_decode_attention", _lib.mp_decode_attention(
         ctypes.byref(cfg), _ptr(tables), _ptr(keys), _ptr(values), n, _ptr(q), _ptr(out), _ptr(scratch),
         scratch_bytes, _stream(stream)))
+
+
+MP_STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def mp_decode_attention_static(cfg: mp_config, tables, keys, values, n: int, q, out, stream=None) -> int:
+    """mp_decode_attention with the library's built-in scratch array (no caller scratch)."""
+    return _check("mp_decode_attention_static", _lib.mp_decode_attention_static(
+        ctypes.byref(cfg), _ptr(tables), _ptr(keys), _ptr(values), n, _ptr(q), _ptr(out), _stream(stream)))
 
 
 def mp_get_status(tables, stream=None) -> int:
