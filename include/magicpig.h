@@ -90,32 +90,39 @@ typedef struct mp_config {
   int32_t dtype;       /* MP_DTYPE_BF16 or MP_DTYPE_F32 (keys, values, q) */
   int32_t w_per_layer; /* 1: W holds one matrix per layer; 0: one matrix shared by all layers */
   int32_t match_mode;  /* MP_MATCH_AUTO, MP_MATCH_CSR or MP_MATCH_SCAN */
-  int32_t threshold;   /* minimum colliding tables for a key to be sampled: 1 or 2 (pages: 2) */
+  int32_t threshold;   /* minimum colliding tables for a key to be sampled, 1..7 (pages: 2);
+                          above 2 it needs L <= 255 and, in CSR mode, capacity <= 196608 */
   int32_t reserved[4]; /* must be zero */
 } mp_config;
 
 /* Byte offsets (from the start of the tables buffer) of the arrays the library keeps
- * between calls. U = layers·batch·kv_heads units, KLp = K·L rounded up to 256,
- * NB = 2^K buckets. Exposed for tests and tools; the contents are library-private. */
+ * between calls. U = layers·batch·kv_heads units, NB = 2^K buckets, TC = columns of
+ * the tile-aligned projection layout: 256-column tiles, each holding floor(256/K)
+ * whole tables (column 256·n + i·K + b is bit b of table n·floor(256/K) + i), the
+ * rest zero. Exposed for tests and tools; the contents are library-private. */
 typedef struct mp_tables_layout {
   uint64_t total_bytes;
   uint64_t header;       /* 256 B: magic, prefill length, appended length, status word */
   uint64_t center;       /* float [U][d]: mean key of tokens [n_sink, n_prefill) */
-  uint64_t beta;         /* float [U][TC]: W^T · center, tensor-core column order */
-  uint64_t wt_f32;       /* float [layers or 1][KLp][d]: W transposed, zero-padded */
-  uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: W transposed in tensor-core column order
-                            (bf16 configs only, else 0) */
+  uint64_t beta;         /* bf16 [U][TC][16]: -W^T·center split into three bf16 terms (elements 0..2,
+                            the rest zero), tile-aligned column order; with `ones` it is the
+                            extra K step of the tensor-core projection that subtracts W^T·center */
+  uint64_t ones;         /* bf16 [128][16]: rows of (1, 1, 1, 0, ..., 0) */
+  uint64_t wt_f32;       /* float [layers or 1][TC][d]: W transposed, tile-aligned column order */
+  uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: the same in bf16 (bf16 configs only, else 0) */
   uint64_t center_parts; /* float [U][parts][d]: partial sums while building */
   uint64_t codes;        /* uint16 [U][L][capacity]: code of every hashed token, table-major */
-  uint64_t csr_offsets;  /* uint32 [U][L][NB+1]: bucket starts in csr_ids, per table (CSR mode, else 0) */
-  uint64_t csr_ids;      /* uint32 [U][L][capacity]: token ids of [n_sink, n_prefill) by bucket, ascending
-                            (CSR mode, else 0) */
+  uint64_t csr_offsets;  /* uint16 [U][L][NS][NB+1]: per table and 32768-token segment of [n_sink, n_prefill),
+                            the start of each bucket within the segment (CSR mode, else 0);
+                            NS = ceil(capacity / 32768) */
+  uint64_t csr_ids;      /* uint16 [U][L][capacity]: element 32768*s + i is the i-th id of segment s in
+                            bucket order, as an offset from the segment's first token; the order inside
+                            a bucket is unspecified (CSR mode, else 0) */
   uint64_t planes;       /* uint32 [U][L][K][CW]: bit-planes, word w bit i = bit b of the code of token
                             32w+i (scan mode, else 0); CW = capacity/32 rounded up to a multiple of 4 */
-  int32_t kl_padded;     /* KLp */
   int32_t n_buckets;     /* NB */
   int32_t parts;
-  int32_t tc_cols;       /* TC: 256-column tiles, each holding floor(256/K) whole tables */
+  int32_t tc_cols;       /* TC */
   int32_t match_mode;    /* the mode in use: MP_MATCH_CSR or MP_MATCH_SCAN (AUTO resolved) */
   int32_t cap_words;     /* CW */
 } mp_tables_layout;

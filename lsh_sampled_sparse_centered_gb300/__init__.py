@@ -51,9 +51,9 @@ class mp_config(ctypes.Structure):
 
 class mp_tables_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
-        "total_bytes", "header", "center", "beta", "wt_f32", "wt_bf16", "center_parts", "codes",
+        "total_bytes", "header", "center", "beta", "ones", "wt_f32", "wt_bf16", "center_parts", "codes",
         "csr_offsets", "csr_ids", "planes")] + [(n, ctypes.c_int32) for n in (
-        "kl_padded", "n_buckets", "parts", "tc_cols", "match_mode", "cap_words")]
+        "n_buckets", "parts", "tc_cols", "match_mode", "cap_words")]
 
 
 class mp_decode_layout(ctypes.Structure):

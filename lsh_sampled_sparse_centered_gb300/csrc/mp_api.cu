@@ -12,6 +12,18 @@ namespace mp {
 
 static uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255u); }
 
+// AUTO: the mode that moves fewer bytes per query head and decode step.
+//   CSR : L buckets of ~m/2^K ids (2 B) + per 32K-token segment 4 B of offsets, per table
+//   SCAN: m tokens x L tables x K bits, read once for the G query heads of a KV head
+static int resolve_match(const mp_config* c) {
+  if (c->match_mode != MP_MATCH_AUTO) return c->match_mode;
+  const double m = std::max(1, c->capacity - c->n_sink - c->window);
+  const double G = double(c->q_heads / c->kv_heads);
+  const double csr = c->L * (m / std::ldexp(1.0, c->K)) * 2.0 + c->L * (4.0 * std::ceil(m / 32768.0) + 2.0);
+  const double scan = m * c->L * c->K / 8.0 / G;
+  return scan < csr ? MP_MATCH_SCAN : MP_MATCH_CSR;
+}
+
 static int check_config(const mp_config* c) {
   if (!c) return MP_ERR_INVALID_ARG;
   if (c->layers < 1 || c->batch < 1 || c->kv_heads < 1 || c->q_heads < 1) return MP_ERR_INVALID_ARG;
@@ -26,23 +38,24 @@ static int check_config(const mp_config* c) {
     if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return MP_ERR_UNSUPPORTED;
   if (c->K > kMaxK || c->L > kMaxL || c->capacity > kMaxCapacity) return MP_ERR_UNSUPPORTED;
-  if (c->threshold > 2) return MP_ERR_UNSUPPORTED;
+  // thresholds above 2: at most 7 (3-bit counters in the scan), L <= 255 (byte counters
+  // in the bucket walk) and, for the bucket walk, one counter byte per token in shared memory
+  if (c->threshold > 7) return MP_ERR_UNSUPPORTED;
+  if (c->threshold > 2 && c->L > 255) return MP_ERR_UNSUPPORTED;
+  if (c->threshold > 2 && resolve_match(c) == MP_MATCH_CSR && c->capacity > kMaxCapacityCounters)
+    return MP_ERR_UNSUPPORTED;
+  if (resolve_match(c) == MP_MATCH_CSR) {
+    // the match kernel keeps per-token bitmaps (or byte counters) and one bucket range
+    // per (table, 32768-token segment) in shared memory
+    const int64_t words = (int64_t(c->capacity) + 31) / 32;
+    const int64_t nseg = (int64_t(c->capacity) + kCsrSeg - 1) / kCsrSeg;
+    const int64_t smem = words * 4 * (c->threshold > 2 ? 9 : 2) + int64_t(c->L) * (nseg * 8 + 2) + 20;
+    if (smem > 227 * 1024) return MP_ERR_UNSUPPORTED;
+  }
   // grid limits: units and queries index blockIdx.x / y
   const int64_t q = int64_t(c->layers) * c->batch * c->q_heads;
   if (q > (1 << 30)) return MP_ERR_UNSUPPORTED;
   return MP_OK;
-}
-
-// AUTO: the mode that moves fewer bytes per query head and decode step.
-//   CSR : L buckets of ~m/2^K ids (4 B) + offsets and code (10 B) per table
-//   SCAN: m tokens x L tables x K bits, read once for the G query heads of a KV head
-static int resolve_match(const mp_config* c) {
-  if (c->match_mode != MP_MATCH_AUTO) return c->match_mode;
-  const double m = std::max(1, c->capacity - c->n_sink - c->window);
-  const double G = double(c->q_heads / c->kv_heads);
-  const double csr = c->L * (m / std::ldexp(1.0, c->K)) * 4.0 + c->L * 10.0;
-  const double scan = m * c->L * c->K / 8.0 / G;
-  return scan < csr ? MP_MATCH_SCAN : MP_MATCH_CSR;
 }
 
 static Geometry geometry(const mp_config* c) {
@@ -64,14 +77,13 @@ static Geometry geometry(const mp_config* c) {
   g.units = c->layers * c->batch * c->kv_heads;
   g.queries = c->layers * c->batch * c->q_heads;
   g.kl = c->K * c->L;
-  g.klp = int(align256(uint64_t(g.kl)));
-  if (g.klp == 0) g.klp = 256;
   g.nb = 1 << c->K;
   g.tpt = c->K > 0 ? 256 / c->K : 0;
   g.nt = c->K > 0 ? (c->L + g.tpt - 1) / g.tpt : 0;
   g.kltc = g.nt * 256;
   g.match = resolve_match(c);
   g.cw = (((c->capacity + 31) / 32) + 3) & ~3;
+  g.nseg = (c->capacity + kCsrSeg - 1) / kCsrSeg;
   g.parts = 32;
   g.n_w = c->w_per_layer ? c->layers : 1;
   return g;
@@ -86,9 +98,11 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
   o->center = off;
   off = align256(off + U * d * 4);
   o->beta = off;
-  off = align256(off + U * uint64_t(g.kltc) * 4);
+  off = align256(off + U * uint64_t(g.kltc) * 16 * 2);
+  o->ones = off;
+  off = align256(off + 128 * 16 * 2);
   o->wt_f32 = off;
-  off = align256(off + uint64_t(g.n_w) * g.klp * d * 4);
+  off = align256(off + uint64_t(g.n_w) * g.kltc * d * 4);
   if (g.dtype == MP_DTYPE_BF16) {
     o->wt_bf16 = off;
     off = align256(off + uint64_t(g.n_w) * g.kltc * d * 2);
@@ -99,15 +113,14 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
   off = align256(off + U * L * cap * 2);
   if (g.match == MP_MATCH_CSR) {
     o->csr_offsets = off;
-    off = align256(off + U * L * (uint64_t(g.nb) + 1) * 4);
+    off = align256(off + U * L * uint64_t(g.nseg) * (uint64_t(g.nb) + 1) * 2);
     o->csr_ids = off;
-    off = align256(off + U * L * cap * 4);
+    off = align256(off + U * L * cap * 2);
   } else {
     o->planes = off;
     off = align256(off + U * L * uint64_t(g.K) * g.cw * 4);
   }
   o->total_bytes = off;
-  o->kl_padded = g.klp;
   o->n_buckets = g.nb;
   o->parts = g.parts;
   o->tc_cols = g.kltc;
@@ -146,13 +159,14 @@ static TablesPtrs tables_ptrs(const Geometry& g, void* base) {
   TablesPtrs t;
   t.hdr = reinterpret_cast<DevHeader*>(b + l.header);
   t.center = reinterpret_cast<float*>(b + l.center);
-  t.beta = reinterpret_cast<float*>(b + l.beta);
+  t.beta = reinterpret_cast<__nv_bfloat16*>(b + l.beta);
+  t.ones = reinterpret_cast<__nv_bfloat16*>(b + l.ones);
   t.wt32 = reinterpret_cast<float*>(b + l.wt_f32);
   t.wt16 = l.wt_bf16 ? reinterpret_cast<__nv_bfloat16*>(b + l.wt_bf16) : nullptr;
   t.cparts = reinterpret_cast<float*>(b + l.center_parts);
   t.codes = reinterpret_cast<uint16_t*>(b + l.codes);
-  t.off = l.csr_offsets ? reinterpret_cast<uint32_t*>(b + l.csr_offsets) : nullptr;
-  t.ids = l.csr_ids ? reinterpret_cast<uint32_t*>(b + l.csr_ids) : nullptr;
+  t.off = l.csr_offsets ? reinterpret_cast<uint16_t*>(b + l.csr_offsets) : nullptr;
+  t.ids = l.csr_ids ? reinterpret_cast<uint16_t*>(b + l.csr_ids) : nullptr;
   t.planes = l.planes ? reinterpret_cast<uint32_t*>(b + l.planes) : nullptr;
   return t;
 }
@@ -200,9 +214,9 @@ static bool use_simt_hash() {
   return e && std::strcmp(e, "simt") == 0;
 }
 
-// Number of split-K slices per query head: enough CTAs to fill the GPU a few times
-// over, but no slice shorter than about 128 list entries (estimated from the
-// closed-form budget at p = 1/2).
+// Number of slices per query head for the attention: about 256 list entries per
+// slice (estimated from the closed-form budget at p = 1/2), at most kSplitsMax. The
+// attention kernel is persistent, so the slices only need to be many and even.
 static int choose_splits(const Geometry& g, int n) {
   const double x = std::ldexp(1.0, -g.K);
   double frac;
@@ -211,10 +225,7 @@ static int choose_splits(const Geometry& g, int n) {
   const int lo = std::min(g.s, n);
   const int hi = std::max(lo, n - g.w);
   const double est = double(n - (hi - lo)) + frac * double(hi - lo);
-  const int by_len = int(std::ceil(est / 128.0));
-  const int target = 8 * device_sm_count();
-  const int by_fill = (target + g.queries - 1) / g.queries;
-  int s = std::min(by_len, by_fill);
+  int s = int(std::ceil(est / 256.0));
   if (s < 1) s = 1;
   if (s > kSplitsMax) s = kSplitsMax;
   return s;
@@ -335,7 +346,13 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
     if (launch_center(g, keys, n_prefill, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   bool done = false;
-  if (g.dtype == MP_DTYPE_BF16 && !use_simt_hash()) {
+  if (g.K == 0) {
+    // no projections: every code of every table is the empty code 0
+    if (cudaMemsetAsync(t.codes, 0, size_t(g.units) * g.L * g.cap * sizeof(uint16_t), st) != cudaSuccess)
+      return MP_ERR_CUDA;
+    done = true;
+  }
+  if (!done && g.dtype == MP_DTYPE_BF16 && !use_simt_hash()) {
     ProfScope ps(st, K_HASH_KEYS_TC);
     if (launch_hash_keys_tc(g, keys, n_prefill, t, st, &done) != cudaSuccess) return MP_ERR_CUDA;
   }
@@ -351,8 +368,8 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
     a.center = t.center;
     a.c_gs = 1;
     a.c_rs = 0;
-    a.wt32 = t.wt32;
-    a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+    a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+    a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
     a.groups_per_w = g.batch * g.kvh;
     a.out = t.codes;
     a.out_gs = int64_t(g.L) * g.cap;
@@ -393,8 +410,8 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   a.center = t.center;
   a.c_gs = g.batch * g.kvh;
   a.c_rs = 1;
-  a.wt32 = t.wt32;
-  a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+  a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+  a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
   a.out = t.codes;
   a.out_gs = int64_t(g.batch) * g.kvh * g.L * g.cap;
@@ -403,6 +420,10 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   // the row index addresses (sequence, KV head); the token is `pos`
   a.src = static_cast<const char*>(keys) + int64_t(pos) * g.d * (g.dtype == MP_DTYPE_BF16 ? 2 : 4);
   a.out = t.codes + pos;
+  // the hash kernel also records the new appended end (no projections when K = 0:
+  // then a one-thread kernel does it)
+  a.mark_hdr = g.nt > 0 ? t.hdr : nullptr;
+  a.mark_pos = pos;
   {
     ProfScope ps(st, K_HASH_APPEND);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
@@ -411,7 +432,7 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
     ProfScope ps(st, K_PLANES_APPEND);
     if (launch_planes_append(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
-  {
+  if (g.nt == 0) {
     ProfScope ps(st, K_MARK_APPENDED);
     if (launch_mark_appended(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
@@ -447,14 +468,17 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   a.groups = g.layers;
   a.row0 = 0;
   a.center = nullptr;
-  a.wt32 = t.wt32;
-  a.w_stride = g.w_per_layer ? int64_t(g.klp) * g.d : 0;
+  a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+  a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
   a.out = dp.qcodes;
   a.out_gs = int64_t(g.batch) * g.qh * g.L;
   a.out_rs = g.L;
   a.out_ts = 1;
-  {
+  if (g.K == 0) {
+    if (cudaMemsetAsync(dp.qcodes, 0, size_t(g.queries) * g.L * sizeof(uint16_t), st) != cudaSuccess)
+      return MP_ERR_CUDA;
+  } else {
     ProfScope ps(st, K_HASH_QUERY);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
   }

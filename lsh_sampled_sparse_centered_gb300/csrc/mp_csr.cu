@@ -1,57 +1,48 @@
-// Hash-table construction: for every (KV head, table) a bucketed id list (CSR)
-// of the prefill tokens [n_sink, n_prefill), keyed by their K-bit code. Within a
-// bucket ids are ascending (stable counting sort).
-// The hash tables HT of MagicPIG (arXiv 2410.16179v2) Algorithm 1 and §4.4(4);
-// the pages build them on the CPU per KV head, here one CTA builds one table.
+// Hash-table construction: for every (KV head, table) the prefill tokens
+// [n_sink, n_prefill) bucketed by their K-bit code, one bucketed segment of up to
+// 32768 tokens at a time (16-bit ids relative to the segment's first token, 16-bit
+// bucket starts). These are the hash tables HT of MagicPIG (arXiv 2410.16179v2)
+// Algorithm 1 and §4.4(4); the pages build them on the CPU per KV head, here one CTA
+// sorts one segment of one table in shared memory and writes it out coalesced. The
+// order of the ids inside a bucket is whatever the shared-memory atomics give: the
+// tables are only ever read as sets.
 #include "mp_internal.h"
 
 namespace mp {
 
-// One CTA per (unit, table). The token range is cut into `nseg` contiguous segments,
-// one per warp. Pass 1: per-warp bucket histograms in shared memory. Then per bucket
-// the segment prefix and the bucket starts (exclusive scan). Pass 2: each warp walks
-// its segment in order and scatters ids; __match_any_sync ranks equal codes inside a
-// 32-token step, so the order of ids within a bucket is the token order.
-__global__ void __launch_bounds__(512) k_csr_build(const uint16_t* __restrict__ codes,
-                                                   uint32_t* __restrict__ off, uint32_t* __restrict__ ids,
-                                                   int L, int cap, int nb, int lo, int hi) {
-  extern __shared__ uint32_t sm[];
-  const int nseg = blockDim.x >> 5;
-  uint32_t* hist = sm;                 // [nseg][nb]
-  uint32_t* scan = sm + nseg * nb;     // [blockDim.x] per-thread partial sums
-  const int64_t table = blockIdx.x;    // unit * L + t
-  const uint16_t* c = codes + table * cap;
-  uint32_t* o = off + table * (nb + 1);
-  uint32_t* id = ids + table * cap;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n = hi - lo;
-  const int span = (n + nseg - 1) / nseg;
-  const int s0 = lo + warp * span, s1 = min(hi, s0 + span);
+constexpr int kCsrThreads = 1024;
 
-  for (int i = threadIdx.x; i < nseg * nb; i += blockDim.x) hist[i] = 0;
+// One CTA per (unit x table, segment). Pass 1: bucket counts with shared-memory atomics.
+// Block scan of the counts gives the bucket starts (written out as the offsets). Pass 2:
+// every token takes a slot of its bucket with a shared-memory atomic on the bucket's
+// cursor. The segment's ids then leave shared memory with consecutive threads on
+// consecutive elements.
+__global__ void __launch_bounds__(kCsrThreads, 2) k_csr_build(const uint16_t* __restrict__ codes,
+                                                           uint16_t* __restrict__ off, uint16_t* __restrict__ ids,
+                                                           int cap, int nb, int nseg, int lo, int hi) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  const int64_t table = blockIdx.x;  // unit * L + t
+  const int s = blockIdx.y;
+  const int a = lo + s * kCsrSeg;
+  const int m = min(hi, a + kCsrSeg) - a;  // tokens of this segment (>= 1)
+  uint32_t* cursor = reinterpret_cast<uint32_t*>(smraw);           // [nb]
+  uint16_t* sorted = reinterpret_cast<uint16_t*>(cursor + nb);     // [kCsrSeg] local ids in bucket order
+  __shared__ uint32_t wsum[kCsrThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t* c = codes + table * cap + a;
+
+  for (int i = tid; i < nb; i += kCsrThreads) cursor[i] = 0u;
   __syncthreads();
-  uint32_t* h = hist + warp * nb;
-  for (int tok = s0 + lane; tok < s1; tok += 32) atomicAdd(&h[c[tok]], 1u);
+  // pass 1 reads the codes from HBM; pass 2 reads them again, from L2
+#pragma unroll 8
+  for (int i = tid; i < m; i += kCsrThreads) atomicAdd(&cursor[c[i]], 1u);
   __syncthreads();
 
-  // per bucket: exclusive prefix over the segments; each thread owns `per`
-  // consecutive buckets and keeps their totals in `scan` for the block scan below
-  const int per = (nb + blockDim.x - 1) / blockDim.x;
-  const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
+  // exclusive scan of the counts: thread i owns buckets [i*per, (i+1)*per)
+  const int per = (nb + kCsrThreads - 1) / kCsrThreads;
+  const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
   uint32_t local = 0;
-  for (int b = b0; b < b1; ++b) {
-    uint32_t run = 0;
-    for (int s = 0; s < nseg; ++s) {
-      const uint32_t v = hist[s * nb + b];
-      hist[s * nb + b] = run;
-      run += v;
-    }
-    local += run;
-    scan[b] = run;  // bucket total
-  }
-  __syncthreads();
-  // block exclusive scan of `local` (per-thread totals)
-  __shared__ uint32_t wsum[32];
+  for (int b = b0; b < b1; ++b) local += cursor[b];
   uint32_t x = local;
 #pragma unroll
   for (int k = 1; k < 32; k <<= 1) {
@@ -61,62 +52,42 @@ __global__ void __launch_bounds__(512) k_csr_build(const uint16_t* __restrict__ 
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t v = lane < nseg ? wsum[lane] : 0;
+    uint32_t v = wsum[lane];
 #pragma unroll
     for (int k = 1; k < 32; k <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, v, k);
       if (lane >= k) v += y;
     }
-    if (lane < nseg) wsum[lane] = v;
+    wsum[lane] = v;
   }
   __syncthreads();
-  uint32_t base = x - local + (warp > 0 ? wsum[warp - 1] : 0);
+  uint16_t* o = off + (table * nseg + s) * int64_t(nb + 1);
+  uint32_t base = x - local + (warp > 0 ? wsum[warp - 1] : 0u);
   for (int b = b0; b < b1; ++b) {
-    const uint32_t total = scan[b];
-    o[b] = base;
-    for (int s = 0; s < nseg; ++s) hist[s * nb + b] += base;
-    base += total;
+    const uint32_t cnt = cursor[b];
+    cursor[b] = base;
+    o[b] = uint16_t(base);
+    base += cnt;
   }
-  if (threadIdx.x == 0) o[nb] = uint32_t(n);
+  if (tid == 0) o[nb] = uint16_t(m);
   __syncthreads();
 
-  // pass 2: stable scatter
-  for (int t0 = s0; t0 < s1; t0 += 32) {
-    const int tok = t0 + lane;
-    const bool act = tok < s1;
-    const unsigned mask = __ballot_sync(0xffffffffu, act);
-    if (act) {
-      const uint32_t code = c[tok];
-      const unsigned peers = __match_any_sync(mask, code);
-      const int leader = __ffs(peers) - 1;
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      uint32_t pos = 0;
-      if (lane == leader) {
-        pos = h[code];
-        h[code] = pos + __popc(peers);
-      }
-      pos = __shfl_sync(peers, pos, leader);
-      id[pos + rank] = uint32_t(tok);
-    }
-    __syncwarp();
-  }
+  // pass 2: placement
+#pragma unroll 8
+  for (int i = tid; i < m; i += kCsrThreads) sorted[atomicAdd(&cursor[__ldcs(&c[i])], 1u)] = uint16_t(i);
+  __syncthreads();
+  uint16_t* dst = ids + table * cap + int64_t(s) * kCsrSeg;
+  for (int i = tid; i < m; i += kCsrThreads) dst[i] = sorted[i];
 }
 
 cudaError_t launch_csr_build(const Geometry& g, int n_prefill, const TablesPtrs& t, cudaStream_t st) {
   const int lo = min(g.s, n_prefill), hi = n_prefill;
-  // segments (warps): as many as fit 200 KB of histograms, at most 16
-  // `scan` holds one slot per bucket, rounded up to whole per-thread chunks
-  auto smem_for = [&](int ns) {
-    const int th = 32 * ns;
-    const int per = (g.nb + th - 1) / th;
-    return (size_t(ns) * g.nb + size_t(per) * th) * sizeof(uint32_t);
-  };
-  int nseg = 16;
-  while (nseg > 1 && smem_for(nseg) > 200 * 1024) --nseg;
-  const int threads = 32 * nseg;
-  const size_t smem = smem_for(nseg);
+  if (hi <= lo) return cudaSuccess;
+  const int segs = (hi - lo + kCsrSeg - 1) / kCsrSeg;
+  const size_t smem = size_t(g.nb) * 4 + size_t(kCsrSeg) * 2;
   cudaFuncSetAttribute(k_csr_build, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  k_csr_build<<<int64_t(g.units) * g.L, threads, smem, st>>>(t.codes, t.off, t.ids, g.L, g.cap, g.nb, lo, hi);
+  dim3 grid(g.units * g.L, segs);
+  k_csr_build<<<grid, kCsrThreads, smem, st>>>(t.codes, t.off, t.ids, g.cap, g.nb, g.nseg, lo, hi);
   return cudaGetLastError();
 }
 

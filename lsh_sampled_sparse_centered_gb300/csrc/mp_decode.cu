@@ -1,8 +1,12 @@
 // Decode step: sampled-set construction from the bucketed tables, then the
 // importance-weighted attention over the sampled keys plus the exact sink/window
 // tokens, split across CTAs with a fused log-sum-exp combine.
+// (A shared-memory-staged variant with one bulk asynchronous copy per K/V row was
+// measured 1.4x slower than the register gathers below on the 96K workload and removed.)
 // MagicPIG (arXiv 2410.16179v2): Algorithm 1, Eq. 9-11, §4.4 "On-device cache".
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "mp_compact.cuh"
 #include "mp_internal.h"
@@ -19,20 +23,28 @@ namespace mp {
 __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
-                                                   const uint32_t* __restrict__ off,
-                                                   const uint32_t* __restrict__ ids, uint32_t* __restrict__ lists,
+                                                   const uint16_t* __restrict__ off,
+                                                   const uint16_t* __restrict__ ids, uint32_t* __restrict__ lists,
                                                    int32_t* __restrict__ list_len, int32_t* __restrict__ sample_count,
                                                    uint32_t* __restrict__ counters, int n, int s, int w, int L,
-                                                   int nb, int cap, int group, int threshold) {
+                                                   int nb, int cap, int nseg, int group, int threshold) {
   extern __shared__ uint32_t sm[];
   const int qh = blockIdx.x;
   const int unit = qh / group;  // [layer][batch][q_head] -> [layer][batch][kv_head]
   const int lo = min(s, n);
   const int hi = max(lo, n - w);
   const int nwords = (hi + 31) >> 5;
+  // threshold <= 2: two bitmaps (met in >= 1 table, in >= 2 tables);
+  // threshold >= 3: one byte counter per token (L <= 255), then a selection bitmap
+  const bool bytes = threshold >= 3;
   uint32_t* seen1 = sm;
   uint32_t* seen2 = sm + nwords;
-  uint16_t* qc = reinterpret_cast<uint16_t*>(sm + 2 * nwords);
+  uint32_t* cnt = sm + nwords;  // [nwords * 8] byte counters (threshold >= 3)
+  const int body = bytes ? nwords * 9 : nwords * 2;
+  uint32_t* bstart = sm + body;          // [L * nseg]: bucket start in the unit's id arrays
+  uint32_t* bsize = bstart + L * nseg;   // [L * nseg + 1]: sizes, then their exclusive scan
+  uint16_t* qc = reinterpret_cast<uint16_t*>(bsize + L * nseg + 1);
+  __shared__ uint32_t wtot[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   const bool built = hdr->magic == kMagic;
@@ -43,46 +55,125 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
     if (!built) atomicOr(&hdr->status, MP_STATUS_NOT_BUILT);
     else if (hi > app_end) atomicOr(&hdr->status, MP_STATUS_APPEND_GAP);
   }
-  for (int i = threadIdx.x; i < 2 * nwords; i += blockDim.x) sm[i] = 0u;
+  for (int i = threadIdx.x; i < body; i += blockDim.x) sm[i] = 0u;
   for (int t = threadIdx.x; t < L; t += blockDim.x) qc[t] = qcodes[int64_t(qh) * L + t];
   __syncthreads();
 
   if (built && hi > lo) {
-    // tokens hashed at build time: walk the query's bucket in every table
+    // tokens hashed at build time: the query's bucket in every (table, segment). The
+    // bucket ranges are fetched first (one round trip for all of them), then a block
+    // scan of their sizes numbers all bucket entries 0 .. total-1, and the threads walk
+    // that flat range 8 entries at a time (8 independent id loads in flight each),
+    // finding an entry's bucket by binary search over the scanned sizes.
     const int64_t tbase = int64_t(unit) * L;
-    for (int t = warp; t < L; t += 8) {
-      const uint32_t* o = off + (tbase + t) * (nb + 1);
+    const int lo_b = min(s, n0);  // first token bucketed at build time
+    const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
+    const int pairs = L * nsu;
+    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
+      const int t = p / nsu, sg = p - (p / nsu) * nsu;
+      const uint16_t* o = off + ((tbase + t) * nseg + sg) * (nb + 1);
       const int code = qc[t];
-      const uint32_t b0 = o[code], b1 = o[code + 1];
-      const uint32_t* id = ids + (tbase + t) * cap;
-      for (uint32_t i = b0 + lane; i < b1; i += 32) {
-        const uint32_t tok = id[i];
+      const uint32_t b0 = __ldg(&o[code]), b1 = __ldg(&o[code + 1]);
+      // absolute position of the bucket in the table's id array
+      bstart[p] = uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0;
+      bsize[p] = b1 - b0;
+    }
+    __syncthreads();
+    // exclusive scan of bsize in place (thread i owns pairs [i*per, (i+1)*per))
+    {
+      const int per = (pairs + blockDim.x - 1) / blockDim.x;
+      const int p0 = min(pairs, int(threadIdx.x) * per), p1 = min(pairs, p0 + per);
+      uint32_t local = 0;
+      for (int p = p0; p < p1; ++p) local += bsize[p];
+      uint32_t x = local;
+#pragma unroll
+      for (int k = 1; k < 32; k <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, k);
+        if (lane >= k) x += y;
+      }
+      if (lane == 31) wtot[warp] = x;
+      __syncthreads();
+      uint32_t run = x - local;
+      for (int k = 0; k < warp; ++k) run += wtot[k];
+      for (int p = p0; p < p1; ++p) {
+        const uint32_t v = bsize[p];
+        bsize[p] = run;
+        run += v;
+      }
+      if (threadIdx.x == blockDim.x - 1) bsize[pairs] = run;
+    }
+    __syncthreads();
+    const uint32_t total = bsize[pairs];
+    const uint16_t* idu = ids + tbase * cap;
+    constexpr int kIn = 8;
+    for (uint32_t f0 = threadIdx.x; f0 < total; f0 += kIn * blockDim.x) {
+      uint32_t tk[kIn];
+#pragma unroll
+      for (int j = 0; j < kIn; ++j) {
+        const uint32_t f = f0 + j * blockDim.x;
+        tk[j] = 0xffffffffu;
+        if (f < total) {
+          // last pair whose first entry is <= f
+          int l = 0, r = pairs - 1;
+          while (l < r) {
+            const int mid = (l + r + 1) >> 1;
+            if (bsize[mid] <= f) l = mid;
+            else r = mid - 1;
+          }
+          const uint32_t sg = (l - (l / nsu) * nsu);
+          tk[j] = uint32_t(lo_b) + sg * kCsrSeg + __ldg(&idu[bstart[l] + (f - bsize[l])]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kIn; ++j) {
+        const uint32_t tok = tk[j];
         if (tok < uint32_t(hi)) {
-          const uint32_t bit = 1u << (tok & 31);
-          const uint32_t old = atomicOr(&seen1[tok >> 5], bit);
-          if (old & bit) atomicOr(&seen2[tok >> 5], bit);
+          if (bytes) {
+            atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
+          } else {
+            const uint32_t bit = 1u << (tok & 31);
+            const uint32_t old = atomicOr(&seen1[tok >> 5], bit);
+            if (old & bit) atomicOr(&seen2[tok >> 5], bit);
+          }
         }
       }
     }
     // tokens appended after the build that have left the window: compare codes
     const int a0 = max(lo, n0), a1 = min(hi, app_end);
     for (int tok = a0 + warp; tok < a1; tok += 8) {
-      int cnt = 0;
-      for (int t = lane; t < L; t += 32)
-        cnt += (codes[(tbase + t) * cap + tok] == qc[t]) ? 1 : 0;
+      int c = 0;
+      for (int t = lane; t < L; t += 32) c += (codes[(tbase + t) * cap + tok] == qc[t]) ? 1 : 0;
 #pragma unroll
-      for (int k = 16; k > 0; k >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, k);
+      for (int k = 16; k > 0; k >>= 1) c += __shfl_xor_sync(0xffffffffu, c, k);
       if (lane == 0) {
-        const uint32_t bit = 1u << (tok & 31);
-        if (cnt >= 1) atomicOr(&seen1[tok >> 5], bit);
-        if (cnt >= 2) atomicOr(&seen2[tok >> 5], bit);
+        if (bytes) {
+          atomicAdd(&cnt[tok >> 2], uint32_t(min(c, 255)) << (8 * (tok & 3)));
+        } else {
+          const uint32_t bit = 1u << (tok & 31);
+          if (c >= 1) atomicOr(&seen1[tok >> 5], bit);
+          if (c >= 2) atomicOr(&seen2[tok >> 5], bit);
+        }
       }
     }
   }
   __syncthreads();
-
+  if (bytes) {
+    // selection bitmap: counter >= threshold (reuses the first nwords words)
+    for (int wi = threadIdx.x; wi < nwords; wi += blockDim.x) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t c4 = cnt[wi * 8 + j];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (((c4 >> (8 * k)) & 0xFFu) >= uint32_t(threshold)) m |= 1u << (4 * j + k);
+      }
+      seen1[wi] = m;
+    }
+    __syncthreads();
+  }
   // compaction of [lo, hi)
-  write_list(threshold >= 2 ? seen2 : seen1, built, lo, hi, n, lists + int64_t(qh) * cap, &sample_count[qh],
+  write_list(threshold == 2 ? seen2 : seen1, built, lo, hi, n, lists + int64_t(qh) * cap, &sample_count[qh],
              &list_len[qh]);
 }
 
@@ -91,312 +182,370 @@ cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, cons
   const int lo = min(g.s, n);
   const int hi = max(lo, n - g.w);
   const int nwords = (hi + 31) >> 5;
-  const size_t smem = size_t(2 * nwords) * 4 + size_t(g.L) * 2 + 16;
+  const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
+  const size_t smem = size_t(body) * 4 + size_t(g.L) * g.nseg * 8 + 4 + size_t(g.L) * 2 + 16;
   cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  k_match_csr<<<g.queries, 256, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists,
-                                            dp.list_len, dp.sample_count, dp.counters, n, g.s, g.w, g.L,
-                                            g.nb, g.cap, g.group, g.threshold);
+  k_match_csr<<<g.queries, 256, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists, dp.list_len,
+                                            dp.sample_count, dp.counters, n, g.s, g.w, g.L, g.nb, g.cap,
+                                            g.nseg, g.group, g.threshold);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------------
-// inclusion probability u = P[Binomial(L, x) >= T], x = p^K  (Eq. 10 / Eq. 11)
+// inclusion probability u = P[Binomial(L, x) >= T], x = p^K  (Eq. 10 / Eq. 11; T = 2
+// on the pages). The printed closed form 1 - sum_{j<T} C(L,j) x^j (1-x)^(L-j)
+// cancels when L*x is small; there the tail sum_{j>=T} is added term by term instead
+// (ratio of consecutive terms (L-j)/(j+1) * x/(1-x)).
 // ---------------------------------------------------------------------------------
-// The printed closed form cancels when L*x is small; there the tail is summed
-// term by term: C(L,2) x^2 (1-x)^(L-2) * (1 + ratio + ...). Elsewhere
-// 1 - (1-x)^(L-1) (1 + (L-1) x) is evaluated as -expm1(log1p(-x)(L-1) + log1p((L-1)x)).
 __device__ __forceinline__ float inclusion_prob(float x, int L, int threshold) {
   if (x >= 1.f) return 1.f;
   if (x <= 0.f) return 0.f;
   const float Lf = float(L);
   if (threshold <= 1) return -expm1f(Lf * log1pf(-x));
-  if (L < 2) return 0.f;
-  if (Lf * x < 0.1f) {
-    const float r = x / (1.f - x);
-    float term = 0.5f * Lf * (Lf - 1.f) * x * x * expf((Lf - 2.f) * log1pf(-x));
+  if (L < threshold) return 0.f;
+  const float l1x = log1pf(-x);
+  const float r = __fdividef(x, 1.f - x);
+  if (threshold == 2) {
+    if (Lf * x < 0.1f) {
+      // consecutive terms shrink by (L-j)/(j+1) * x/(1-x) < 0.04, so six terms reach
+      // fp32 precision; the unrolled loop has constant reciprocals
+      float term = 0.5f * Lf * (Lf - 1.f) * x * x * expf((Lf - 2.f) * l1x);
+      float sum = term;
+#pragma unroll
+      for (int j = 2; j < 8; ++j) {
+        term *= fmaxf(Lf - float(j), 0.f) * (1.f / float(j + 1)) * r;
+        sum += term;
+      }
+      return sum;
+    }
+    // 1 - (1-x)^(L-1) (1 + (L-1) x)
+    return -expm1f((Lf - 1.f) * l1x + log1pf((Lf - 1.f) * x));
+  }
+  const float T = float(threshold);
+  if (Lf * x < 0.5f * T) {
+    float term = expf(lgammaf(Lf + 1.f) - lgammaf(T + 1.f) - lgammaf(Lf - T + 1.f) + T * logf(x) + (Lf - T) * l1x);
     float sum = term;
-    for (int j = 2; j < L && j < 14; ++j) {
+    for (int j = threshold; j < L && j < threshold + 24; ++j) {
       term *= (Lf - float(j)) / float(j + 1) * r;
       sum += term;
       if (term < 1e-9f * sum) break;
     }
     return sum;
   }
-  return -expm1f((Lf - 1.f) * log1pf(-x) + log1pf((Lf - 1.f) * x));
-}
-
-// ---------------------------------------------------------------------------------
-// bounded mbarrier / bulk-copy helpers (inline PTX)
-// ---------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Returns false if the phase did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  float term = expf(Lf * l1x);
+  float head = term;
+  for (int j = 0; j < threshold - 1; ++j) {
+    term *= (Lf - float(j)) / float(j + 1) * r;
+    head += term;
   }
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+  return 1.f - head;
 }
 
-// ---------------------------------------------------------------------------------
-// attention over list entries, split-K across CTAs, fused combine
-// ---------------------------------------------------------------------------------
-constexpr int kRows = 32;     // list entries per tile
-constexpr int kStages = 2;
 constexpr int kAttThreads = 128;
 
-template <typename T, int D>
-struct AttSmem {
-  T k[kStages][kRows][D];
-  T v[kStages][kRows][D];
-  float logit[kRows];
-  float e[kRows];
-  float red[kAttThreads];
-  uint64_t bar[kStages];
-  int last;
-};
+// ---------------------------------------------------------------------------------
+// attention with register gathers: each warp walks groups of list entries, every
+// lane loading one 16-byte slice of a K row and of a V row (a warp covers 32/LPR rows
+// per load, LPR = lanes per row), so a group of U x RPI rows (U = 8) is in flight per warp
+// without shared-memory staging; the online softmax state (m, l, acc) lives in
+// registers and the warps of a CTA merge through shared memory at the end.
+// ---------------------------------------------------------------------------------
+constexpr int kGatherUnroll = 8;
+constexpr int kListChunk = 1024;
 
-template <typename T>
-__device__ __forceinline__ void load_pair(const T* p, float& a, float& b);
-template <>
-__device__ __forceinline__ void load_pair<__nv_bfloat16>(const __nv_bfloat16* p, float& a, float& b) {
-  const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
-  a = __bfloat162float(v.x);
-  b = __bfloat162float(v.y);
+__device__ __forceinline__ void unpack8(const uint4& v, const __nv_bfloat16*, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(h[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
 }
-template <>
-__device__ __forceinline__ void load_pair<float>(const float* p, float& a, float& b) {
-  const float2 v = *reinterpret_cast<const float2*>(p);
-  a = v.x;
-  b = v.y;
+__device__ __forceinline__ void unpack8(const uint4& v, const float*, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
 }
 
-// One CTA = one slice of one query head's list. Per tile of 32 entries: the K and V
-// rows are gathered into shared memory by bulk asynchronous copies (one 128/256/512-B
-// copy per row, completion counted on an mbarrier), a warp per row forms the logit
-// q.k/sqrt(d) - log u (u = 1 for exact tokens) and an online softmax keeps
-// (m, l, acc[d]). Slices of a head are merged by the CTA that finishes last.
+// Transposed butterfly over the LPR lanes of a row set: on entry s[u] is this lane's
+// partial sum for row u (u < 8) of its sub-group. Three halving steps (lane offsets
+// LPR/2, LPR/4, LPR/8) each exchange half of the remaining rows, leaving every lane one
+// row, ju = 4*[lane & LPR/2] + 2*[lane & LPR/4] + [lane & LPR/8], summed over 8 lanes;
+// the offsets below LPR/8 finish the sum. 7 shuffles for 8 rows instead of 8*log2(LPR).
+template <int LPR>
+__device__ __forceinline__ float reduce_rows8(float (&s)[8], int lane) {
+  static_assert(LPR >= 8 && LPR <= 32, "row sets of 8..32 lanes");
+#pragma unroll
+  for (int lvl = 0; lvl < 3; ++lvl) {
+    const int o = (LPR / 2) >> lvl, half = 4 >> lvl;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = up ? s[j] : s[j + half];
+      const float keep = up ? s[j + half] : s[j];
+      s[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float r = s[0];
+#pragma unroll
+  for (int o = LPR / 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+// the lane of sub-group `sub` that holds row u after reduce_rows8
+template <int LPR>
+__device__ __forceinline__ int row_lane(int sub, int u) {
+  return sub * LPR + (u >> 2) * (LPR / 2) + ((u >> 1) & 1) * (LPR / 4) + (u & 1) * (LPR / 8);
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kAttThreads) k_attend(
-    DevHeader* hdr, const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len,
-    const float* __restrict__ center, const T* __restrict__ keys, const T* __restrict__ values,
-    const T* __restrict__ q, float* __restrict__ out, float* __restrict__ partials, uint32_t* __restrict__ counters,
-    int cap, int group, int K, int L, int threshold) {
-  extern __shared__ __align__(128) unsigned char smraw[];
-  AttSmem<T, D>& S = *reinterpret_cast<AttSmem<T, D>*>(smraw);
-  const int qh = blockIdx.y, split = blockIdx.x, P = gridDim.x;
+__global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
+    const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
+    const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
+    float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
+    int threshold, int P, int queries) {
+  constexpr int VE = 16 / int(sizeof(T));  // elements per 16-byte slice
+  constexpr int LPR = D / VE;              // lanes per row
+  constexpr int RPI = 32 / LPR;            // rows per warp-wide load
+  constexpr int U = kGatherUnroll;
+  static_assert(U == 8, "reduce_rows8 takes 8 rows per lane");
+  constexpr int GR = RPI * U;              // rows per group
+  constexpr int NW = kAttThreads / 32;
+  __shared__ float sm_m[NW], sm_l[NW];
+  __shared__ float sm_acc[NW][D];
+  __shared__ int sm_last;
+  __shared__ uint32_t sl[kListChunk];
+  // persistent: the CTA walks items (query head, slice) = (item / P, item % P)
+  for (int item = blockIdx.x; item < queries * P; item += gridDim.x) {
+  const int qh = item / P, split = item - (item / P) * P;
   const int unit = qh / group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane / LPR, part = lane % LPR;
   const int len = list_len[qh];
   const int per = (len + P - 1) / P;
   const int beg = min(len, split * per), end = min(len, beg + per);
   const uint32_t* lst = lists + int64_t(qh) * cap;
-  const T* kbase = keys + int64_t(unit) * cap * D;
-  const T* vbase = values + int64_t(unit) * cap * D;
-  constexpr uint32_t kRowBytes = D * sizeof(T);
-  constexpr int kPer = D / 64;  // element pairs per lane
+  const T* kbase = keys + int64_t(unit) * cap * D + part * VE;
+  const T* vbase = values + int64_t(unit) * cap * D + part * VE;
 
-  // the lane's share of q and c: elements 2*lane + 64*i, +1
-  float qr[2 * kPer], cr[2 * kPer];
+  float qr[VE], cr[VE];
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int j = 2 * lane + 64 * i;
-    qr[2 * i] = to_f(q[int64_t(qh) * D + j]);
-    qr[2 * i + 1] = to_f(q[int64_t(qh) * D + j + 1]);
-    cr[2 * i] = center[int64_t(unit) * D + j];
-    cr[2 * i + 1] = center[int64_t(unit) * D + j + 1];
+  for (int i = 0; i < VE; ++i) {
+    qr[i] = to_f(q[int64_t(qh) * D + part * VE + i]);
+    cr[i] = center[int64_t(unit) * D + part * VE + i];
   }
-  float qq = 0.f;
+  float qq = 0.f, qc = 0.f;
 #pragma unroll
-  for (int i = 0; i < 2 * kPer; ++i) qq = fmaf(qr[i], qr[i], qq);
+  for (int i = 0; i < VE; ++i) {
+    qq = fmaf(qr[i], qr[i], qq);
+    qc = fmaf(qr[i], cr[i], qc);
+  }
 #pragma unroll
-  for (int k = 16; k > 0; k >>= 1) qq += __shfl_xor_sync(0xffffffffu, qq, k);
+  for (int o = LPR / 2; o >= 1; o >>= 1) {
+    qq += __shfl_xor_sync(0xffffffffu, qq, o);
+    qc += __shfl_xor_sync(0xffffffffu, qc, o);
+  }
   const float qnorm = sqrtf(qq);
+  // this lane's row of the group after reduce_rows8
+  const int ju = 4 * ((lane & (LPR / 2)) != 0) + 2 * ((lane & (LPR / 4)) != 0) + ((lane & (LPR / 8)) != 0);
   const float scale = rsqrtf(float(D));
 
-  if (tid == 0)
-    for (int s = 0; s < kStages; ++s) mbar_init(&S.bar[s], kRows);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  float m_run = -CUDART_INF_F, l_run = 0.f;
+  float acc[VE];
+#pragma unroll
+  for (int i = 0; i < VE; ++i) acc[i] = 0.f;
+
+  // the slice's list entries go through shared memory (one round trip per chunk), so
+  // that each group only waits for its K and V rows
+  for (int c0 = beg; c0 < end; c0 += kListChunk) {
+  const int cn = min(kListChunk, end - c0);
+  for (int i = tid; i < cn; i += kAttThreads) sl[i] = __ldg(&lst[c0 + i]);
   __syncthreads();
-
-  const int ntiles = (end - beg + kRows - 1) / kRows;
-  auto issue = [&](int tile) {
-    const int st = tile % kStages;
-    if (tid < kRows) {
-      const int e = beg + tile * kRows + tid;
-      if (e < end) {
-        const uint32_t tok = lst[e] & ~kExactFlag;
-        mbar_arrive_expect_tx(&S.bar[st], 2 * kRowBytes);
-        bulk_g2s(&S.k[st][tid][0], kbase + int64_t(tok) * D, kRowBytes, &S.bar[st]);
-        bulk_g2s(&S.v[st][tid][0], vbase + int64_t(tok) * D, kRowBytes, &S.bar[st]);
+  const int ngroups = (cn + GR - 1) / GR;
+  for (int gi = warp; gi < ngroups; gi += NW) {
+    const int e0 = gi * GR + sub;
+    uint32_t ent[U];
+    uint4 kv[U], vv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * RPI;
+      ent[u] = e < cn ? sl[e] : 0xffffffffu;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ent[u] != 0xffffffffu) {
+        const int64_t tok = int64_t(ent[u] & ~kExactFlag);
+        kv[u] = __ldg(reinterpret_cast<const uint4*>(kbase + tok * D));
+        vv[u] = __ldg(reinterpret_cast<const uint4*>(vbase + tok * D));
       } else {
-        mbar_arrive(&S.bar[st]);
+        kv[u] = make_uint4(0u, 0u, 0u, 0u);
+        vv[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-  };
-
-  constexpr int RS = kAttThreads / D;  // threads per output dim (1 for d=128, 2 for d=64)
-  const int dim = tid % D, rphase = tid / D;
-  float m_run = -CUDART_INF_F, l_run = 0.f, acc = 0.f;
-
-  if (ntiles > 0) issue(0);
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int st = tile % kStages;
-    if (tile + 1 < ntiles) issue(tile + 1);
-    const bool got = mbar_wait_bounded(&S.bar[st], uint32_t((tile / kStages) & 1));
-    if (__syncthreads_or(!got)) {
-      // give up on this head; wait (bounded) for the copies still in flight so that
-      // none lands after the CTA has released its shared memory
-      if (tid == 0) atomicOr(&hdr->status, MP_STATUS_WAIT_TIMEOUT);
-      (void)mbar_wait_bounded(&S.bar[st], uint32_t((tile / kStages) & 1));
-      if (tile + 1 < ntiles)
-        (void)mbar_wait_bounded(&S.bar[(tile + 1) % kStages], uint32_t(((tile + 1) / kStages) & 1));
-      m_run = -CUDART_INF_F;
-      l_run = 0.f;
-      acc = 0.f;
-      break;
-    }
-    const int nvalid = min(kRows, end - (beg + tile * kRows));
-    // logits: one warp per row
-    for (int r = warp; r < kRows; r += kAttThreads / 32) {
-      float lg = -CUDART_INF_F;
-      if (r < nvalid) {
-        const uint32_t ent = lst[beg + tile * kRows + r];
-        float dot = 0.f, dotc = 0.f, kk = 0.f;
+    // per row: q.k and |k - c|^2 (q.(k - c) = q.k - q.c), reduced so that every lane
+    // ends with one row of the group and evaluates the scalar part of its logit
+    float sa[U], sn[U];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          float k0, k1;
-          load_pair<T>(&S.k[st][r][2 * lane + 64 * i], k0, k1);
-          const float c0 = k0 - cr[2 * i], c1 = k1 - cr[2 * i + 1];
-          dot = fmaf(qr[2 * i], k0, fmaf(qr[2 * i + 1], k1, dot));
-          dotc = fmaf(qr[2 * i], c0, fmaf(qr[2 * i + 1], c1, dotc));
-          kk = fmaf(c0, c0, fmaf(c1, c1, kk));
-        }
+    for (int u = 0; u < U; ++u) {
+      float kf[VE];
+      unpack8(kv[u], static_cast<const T*>(nullptr), kf);
+      float a = 0.f, c = 0.f;
 #pragma unroll
-        for (int k = 16; k > 0; k >>= 1) {
-          dot += __shfl_xor_sync(0xffffffffu, dot, k);
-          dotc += __shfl_xor_sync(0xffffffffu, dotc, k);
-          kk += __shfl_xor_sync(0xffffffffu, kk, k);
-        }
-        lg = dot * scale;
-        if (!(ent & kExactFlag)) {
-          // p = 1 - theta(q, k - c)/pi, u = P[Bin(L, p^K) >= threshold]  (Eq. 10/11)
-          const float kn = sqrtf(kk);
-          float cs = (qnorm > 0.f && kn > 0.f) ? dotc / (qnorm * kn) : 0.f;
-          cs = fminf(1.f, fmaxf(-1.f, cs));
-          const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
-          float x = 1.f;
-          for (int b = 0; b < K; ++b) x *= p;
-          const float u = fmaxf(inclusion_prob(x, L, threshold), 1e-30f);
-          lg -= logf(u);
-        }
+      for (int i = 0; i < VE; ++i) {
+        const float c0 = kf[i] - cr[i];
+        a = fmaf(qr[i], kf[i], a);
+        c = fmaf(c0, c0, c);
       }
-      if (lane == 0) S.logit[r] = lg;
+      sa[u] = a;
+      sn[u] = c;
     }
-    __syncthreads();
-    // online softmax: every thread derives the same max and rescale factor
-    float mt = -CUDART_INF_F;
-    for (int r = 0; r < nvalid; ++r) mt = fmaxf(mt, S.logit[r]);
-    const float m_new = fmaxf(m_run, mt);
+    const float rd = reduce_rows8<LPR>(sa, lane);
+    const float rkk = reduce_rows8<LPR>(sn, lane);
+    const int je = gi * GR + ju * RPI + sub;
+    const uint32_t rent = je < cn ? sl[je] : 0xffffffffu;
+    float lg = -CUDART_INF_F;
+    if (rent != 0xffffffffu) {
+      lg = rd * scale;
+      if (!(rent & kExactFlag)) {
+        // p = 1 - theta(q, k - c)/pi, u = P[Bin(L, p^K) >= threshold]  (Eq. 10/11)
+        const float kn = sqrtf(rkk);
+        float cs = (qnorm > 0.f && kn > 0.f) ? (rd - qc) / (qnorm * kn) : 0.f;
+        cs = fminf(1.f, fmaxf(-1.f, cs));
+        const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
+        // x = p^K by squaring (K <= 12)
+        float x = 1.f, pb = p;
+#pragma unroll
+        for (int bit = 0; bit < 4; ++bit) {
+          if ((K >> bit) & 1) x *= pb;
+          pb *= pb;
+        }
+        lg -= logf(fmaxf(inclusion_prob(x, L, threshold), 1e-30f));
+      }
+    }
+    // group maximum (every row sits in LPR/8 lanes)
+    float mg = lg;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+    const float m_new = fmaxf(m_run, mg);
+    if (m_new == -CUDART_INF_F) continue;  // warp-uniform: nothing valid yet
     const float alpha = (m_run == -CUDART_INF_F) ? 0.f : __expf(m_run - m_new);
-    if (tid < kRows) S.e[tid] = (tid < nvalid && S.logit[tid] != -CUDART_INF_F) ? __expf(S.logit[tid] - m_new) : 0.f;
-    __syncthreads();
-    float esum = 0.f;
-    for (int r = 0; r < nvalid; ++r) esum += S.e[r];
-    l_run = l_run * alpha + esum;
-    m_run = m_new;
-    float a = 0.f;
-    for (int r = rphase; r < nvalid; r += RS) a = fmaf(S.e[r], to_f(S.v[st][r][dim]), a);
-    acc = acc * alpha + a;
-    __syncthreads();
-  }
-  // fold the RS row phases of each dim
-  if (RS > 1) {
-    S.red[tid] = acc;
-    __syncthreads();
-    if (tid < D) {
-      float v = 0.f;
-      for (int r = 0; r < RS; ++r) v += S.red[r * D + tid];
-      acc = v;
+    // each lane's weights for its rows: the row lane's logit, shifted by the new maximum
+    const float pw = (lg == -CUDART_INF_F) ? 0.f : __expf(lg - m_new);
+    float ps = 0.f;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) acc[i] *= alpha;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float p = __shfl_sync(0xffffffffu, pw, row_lane<LPR>(sub, u));
+      ps += p;
+      float vf[VE];
+      unpack8(vv[u], static_cast<const T*>(nullptr), vf);
+#pragma unroll
+      for (int i = 0; i < VE; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
     }
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    l_run = l_run * alpha + ps;
+    m_run = m_new;
+  }
+  __syncthreads();  // before the next chunk overwrites the staged entries
+  }
+  // rows of the other sub-groups of lanes hold the same dims: fold them
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < VE; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  if (lane < LPR)
+#pragma unroll
+    for (int i = 0; i < VE; ++i) sm_acc[warp][part * VE + i] = acc[i];
+  if (lane == 0) {
+    sm_m[warp] = m_run;
+    sm_l[warp] = l_run;
+  }
+  __syncthreads();
+  // merge the warps of this CTA
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w]);
+  float f[NW];
+  float lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    f[w] = (sm_m[w] == -CUDART_INF_F) ? 0.f : __expf(sm_m[w] - M);
+    lt = fmaf(sm_l[w], f[w], lt);
   }
   if (P == 1) {
-    if (tid < D) out[int64_t(qh) * D + tid] = (l_run > 0.f) ? acc / l_run : 0.f;
-    return;
+    for (int dd = tid; dd < D; dd += kAttThreads) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) a = fmaf(sm_acc[w][dd], f[w], a);
+      out[int64_t(qh) * D + dd] = lt > 0.f ? a / lt : 0.f;
+    }
+    __syncthreads();  // shared state is reused by the next item
+    continue;
   }
-  float* part = partials + (int64_t(qh) * kSplitsMax + split) * (D + 2);
-  if (tid < D) part[2 + tid] = acc;
+  float* part_out = partials + (int64_t(qh) * kSplitsMax + split) * (D + 2);
+  for (int dd = tid; dd < D; dd += kAttThreads) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) a = fmaf(sm_acc[w][dd], f[w], a);
+    part_out[2 + dd] = a;
+  }
   if (tid == 0) {
-    part[0] = m_run;
-    part[1] = l_run;
+    part_out[0] = M;
+    part_out[1] = lt;
   }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     const uint32_t done = atomicAdd(&counters[qh], 1u);
-    S.last = (done == uint32_t(P - 1)) ? 1 : 0;
+    sm_last = (done == uint32_t(P - 1)) ? 1 : 0;
   }
   __syncthreads();
-  if (!S.last) return;
-  __threadfence();
-  if (tid < D) {
+  if (sm_last) {
+    __threadfence();
     const float* base = partials + int64_t(qh) * kSplitsMax * (D + 2);
-    float M = -CUDART_INF_F;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, __ldcg(&base[p * (D + 2)]));
-    float lt = 0.f, at = 0.f;
-    if (M != -CUDART_INF_F) {
-      for (int p = 0; p < P; ++p) {
-        const float mp = __ldcg(&base[p * (D + 2)]);
-        if (mp == -CUDART_INF_F) continue;
-        const float f = __expf(mp - M);
-        lt = fmaf(__ldcg(&base[p * (D + 2) + 1]), f, lt);
-        at = fmaf(__ldcg(&base[p * (D + 2) + 2 + tid]), f, at);
+    float MM = -CUDART_INF_F;
+    for (int p = 0; p < P; ++p) MM = fmaxf(MM, __ldcg(&base[p * (D + 2)]));
+    for (int dd = tid; dd < D; dd += kAttThreads) {
+      float l2 = 0.f, a2 = 0.f;
+      if (MM != -CUDART_INF_F) {
+        for (int p = 0; p < P; ++p) {
+          const float mp = __ldcg(&base[p * (D + 2)]);
+          if (mp == -CUDART_INF_F) continue;
+          const float fp = __expf(mp - MM);
+          l2 = fmaf(__ldcg(&base[p * (D + 2) + 1]), fp, l2);
+          a2 = fmaf(__ldcg(&base[p * (D + 2) + 2 + dd]), fp, a2);
+        }
       }
+      out[int64_t(qh) * D + dd] = l2 > 0.f ? a2 / l2 : 0.f;
     }
-    out[int64_t(qh) * D + tid] = lt > 0.f ? at / lt : 0.f;
+    if (tid == 0) counters[qh] = 0u;
   }
-  if (tid == 0) counters[qh] = 0u;
+  __syncthreads();  // shared state is reused by the next item
+  }
 }
 
 template <typename T, int D>
 static cudaError_t launch_attend_t(const Geometry& g, int splits, const TablesPtrs& t, const void* keys,
                                    const void* values, const void* q, float* out, const DecodePtrs& dp,
                                    cudaStream_t st) {
-  const size_t smem = sizeof(AttSmem<T, D>);
-  cudaFuncSetAttribute(k_attend<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  dim3 grid(splits, g.queries);
-  k_attend<T, D><<<grid, kAttThreads, smem, st>>>(
-      t.hdr, dp.lists, dp.list_len, t.center, static_cast<const T*>(keys), static_cast<const T*>(values),
-      static_cast<const T*>(q), out, dp.partials, dp.counters, g.cap, g.group, g.K, g.L, g.threshold);
+  // persistent grid: as many CTAs as can be resident at once, each walking items
+  static int per_sm[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& occ = per_sm[dev & 63];
+  if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attend_gather<T, D>, kAttThreads, 0) !=
+                       cudaSuccess ||
+                   occ < 1))
+    occ = 1;
+  const int64_t items = int64_t(splits) * g.queries;
+  const int grid = int(std::min<int64_t>(items, int64_t(occ) * device_sm_count()));
+  k_attend_gather<T, D><<<grid, kAttThreads, 0, st>>>(
+      dp.lists, dp.list_len, t.center, static_cast<const T*>(keys), static_cast<const T*>(values),
+      static_cast<const T*>(q), out, dp.partials, dp.counters, g.cap, g.group, g.K, g.L, g.threshold, splits,
+      g.queries);
   return cudaGetLastError();
 }
 

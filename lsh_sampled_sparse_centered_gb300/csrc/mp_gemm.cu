@@ -1,9 +1,11 @@
 // SimHash of bf16 prefill keys on the 5th-generation tensor cores (tcgen05).
 //
-// For every unit (layer, sequence, KV head) the projections Y = K_u W (keys
-// [n_prefill, d] times W [d, K*L]) run as a bf16 GEMM with fp32 accumulation in
-// tensor memory; the epilogue subtracts beta = W^T c (centering, MagicPIG arXiv
-// 2410.16179v2 §4.3 "Data pre-processing"), keeps the sign of each projection and
+// For every unit (layer, sequence, KV head) the centered projections
+// Y = (K_u - c) W = K_u W - beta (keys [n_prefill, d], W [d, K*L], beta = W^T c;
+// centering: MagicPIG arXiv 2410.16179v2 §4.3 "Data pre-processing") run as a bf16
+// GEMM with fp32 accumulation in tensor memory. -beta enters the accumulator through
+// one extra K step: a tile of rows (1, 1, 1, 0, ...) times the per-unit split of -beta
+// into three bf16 terms (exact). The epilogue keeps the sign of each projection and
 // packs K signs into each table's code (§2.2 SimHash, §4.3 "Hash function selection").
 // bf16 x bf16 products are exact in fp32, so with bf16-representable W the only
 // rounding is the fp32 accumulation.
@@ -11,7 +13,8 @@
 // Structure: persistent CTAs, one per SM, each walking 128-key tiles. Warp 0 streams
 // key tiles (A, 128 x d) and W column tiles (B, 256 x d) with TMA into 128B-swizzled
 // shared memory; warp 1 issues tcgen05.mma (M=128, N=256, K=16 steps) into one of two
-// 256-column fp32 accumulators in tensor memory; warps 2..9 read the accumulator with
+// 256-column fp32 accumulators in tensor memory; warps 2..13 (three per tensor-memory
+// lane quarter, each owning a third of the tile's tables) read the accumulator with
 // tcgen05.ld, form the codes and store them. W columns are laid out so that every
 // 256-column tile holds floor(256/K) whole tables: no code straddles two tiles.
 // All waits are bounded: on expiry the kernel records MP_STATUS_WAIT_TIMEOUT and stops.
@@ -26,8 +29,8 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 12;  // three per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -43,12 +46,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");
 }
+// try_wait with a suspend-time hint (ns): a waiting thread sleeps until the phase
+// completes or the hint expires instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(saddr(bar)), "r"(parity)
+      : "r"(saddr(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -86,6 +91,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   d |= uint64_t(2) << 61;
   return d;
 }
+// K-major operand of one K step (16 bf16 = 32 B per row) in the TMA SWIZZLE_32B layout:
+// 8-row atoms 256 B apart.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= uint64_t((addr & 0x3FFFFu) >> 4);
+  d |= uint64_t(1) << 16;
+  d |= uint64_t(256 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(6) << 61;
+  return d;
+}
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -109,7 +125,56 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Sign bits of 32 accumulator columns: bit j <-> column j is 1 iff y_j >= +0, i.e.
+// y - beta > 0 up to an exact zero, which lies in the near-tie band. Four independent
+// shift chains (columns j, j+8, j+16, j+24) keep the dependency chains short.
+__device__ __forceinline__ uint32_t sign_word(const uint32_t (&r)[32]) {
+  uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w0 = __funnelshift_l(r[i], w0, 1);
+    w1 = __funnelshift_l(r[8 + i], w1, 1);
+    w2 = __funnelshift_l(r[16 + i], w2, 1);
+    w3 = __funnelshift_l(r[24 + i], w3, 1);
+  }
+  // w_k holds the sign bits of columns 8k..8k+7, column 8k at bit 7
+  return ~__brev((w0 << 24) | (w1 << 16) | (w2 << 8) | w3);
+}
+
+// Codes of one third of a 256-column tile with K known at compile time: the column,
+// word and shift of every code are constants, so cutting a code is one or two shifts.
+template <int KC, int THIRD>
+__device__ __forceinline__ void epi_tile_k(uint32_t tbase, uint16_t* codes, int64_t u, int L, int cap, int row,
+                                           bool store, int n) {
+  constexpr int TPT = 256 / KC;
+  constexpr int TP = (TPT + 2) / 3;
+  constexpr int TL0 = (THIRD * TP < TPT) ? THIRD * TP : TPT;
+  constexpr int TL1 = (TL0 + TP < TPT) ? TL0 + TP : TPT;
+  if constexpr (TL0 < TL1) {
+    constexpr int C0 = TL0 * KC, C1 = TL1 * KC;
+    constexpr int CH0 = C0 / 32, CH1 = (C1 - 1) / 32, NCH = CH1 - CH0 + 1;
+    uint32_t words[NCH + 1];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      uint32_t r0[32];
+      tmem_ld32(tbase + uint32_t((CH0 + i) * 32), r0);
+      tmem_wait_ld();
+      words[i] = sign_word(r0);
+    }
+    words[NCH] = 0u;
+    constexpr uint32_t MASK = (1u << KC) - 1u;
+#pragma unroll
+    for (int tl = TL0; tl < TL1; ++tl) {
+      const int c = tl * KC, wi = c / 32 - CH0, sh = c % 32;
+      uint32_t code = words[wi] >> sh;
+      if (sh + KC > 32) code |= words[wi + 1] << (32 - sh);
+      const int t = n * TPT + tl;
+      if (store && t < L) codes[(u * L + t) * cap + row] = uint16_t(code & MASK);
+    }
+  }
 }
 
 template <int D>
@@ -118,23 +183,27 @@ struct GemmSmem {
   // A: [2 slots][kSub][128 rows][64], B: [2 slots][kSub][256 rows][64]; every sub-tile 1024-aligned
   __nv_bfloat16 a[2][kSub][kTileM * 64];
   __nv_bfloat16 b[2][kSub][kTileN * 64];
-  uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2];
+  __nv_bfloat16 b1[2][kTileN * 16];  // -beta split of the stage's columns (32-byte swizzle)
+  __nv_bfloat16 a1[kTileM * 16];     // rows (1, 1, 1, 0, ...) (32-byte swizzle)
+  uint64_t a_full[2], a_empty[2], b_full[2], b_empty[2], acc_full[2], acc_empty[2], ones_full;
   uint32_t tmem_base;
   uint32_t abort;
 };
 
-template <int D>
+template <int D, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_hash_keys_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmW,
-                   const float* __restrict__ beta, uint16_t* __restrict__ codes, DevHeader* hdr, int units,
-                   int units_per_w, int w_per_layer, int cap, int n0, int L, int K, int tpt, int nt) {
+                   const __grid_constant__ CUtensorMap tmBias, const __grid_constant__ CUtensorMap tmOnes,
+                   uint16_t* __restrict__ codes, DevHeader* hdr, int units,
+                   int units_per_w, int w_per_layer, int cap, int n0, int L, int K, int tpt, int nt, int kltc) {
   extern __shared__ __align__(1024) unsigned char smraw[];
   // align the dynamic shared memory to 1024 B for the swizzle atoms
   const uint32_t base = saddr(smraw);
   GemmSmem<D>& S = *reinterpret_cast<GemmSmem<D>*>(smraw + ((1024 - (base & 1023)) & 1023));
   constexpr int kSub = GemmSmem<D>::kSub;
   constexpr uint32_t kABytes = kTileM * D * 2;
-  constexpr uint32_t kBBytes = kTileN * D * 2;
+  constexpr uint32_t kBBytes = kTileN * D * 2 + kTileN * 16 * 2;  // W columns + their -beta split
+  constexpr uint32_t kOnesBytes = kTileM * 16 * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (n0 + kTileM - 1) / kTileM;
   const int items = units * mt;
@@ -149,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.acc_full[i], 1);
       mbar_init(&S.acc_empty[i], kEpiWarps);
     }
+    mbar_init(&S.ones_full, 1);
     S.abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -166,6 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      mbar_expect_tx(&S.ones_full, kOnesBytes);
+      tma_load_2d(&S.a1[0], &tmOnes, 0, 0, &S.ones_full);
       uint32_t bc = 0;
       int li = 0;
       for (int item = blockIdx.x; item < items && !*abort; item += gridDim.x, ++li) {
@@ -185,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&S.b_full[bs], kBBytes);
           for (int s = 0; s < kSub; ++s)
             tma_load_2d(&S.b[bs][s][0], &tmW, s * 64, wrow + n * kTileN, &S.b_full[bs]);
+          tma_load_2d(&S.b1[bs][0], &tmBias, 0, u * kltc + n * kTileN, &S.b_full[bs]);
         }
         if (!ok) break;
       }
@@ -196,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              (uint32_t(kTileM >> 4) << 24);
       uint32_t bc = 0, ac = 0;
       int li = 0;
-      for (int item = blockIdx.x; item < items && !*abort; item += gridDim.x, ++li) {
+      const bool have_ones = mbar_wait(&S.ones_full, 0, abort);
+      for (int item = blockIdx.x; have_ones && item < items && !*abort; item += gridDim.x, ++li) {
         const int as = li & 1;
         if (!mbar_wait(&S.a_full[as], (li >> 1) & 1, abort)) break;
         fence_after();
@@ -217,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t db = sw128_desc(saddr(&S.b[bs][s][0]) + off);
             mma_bf16(d_tmem, da, db, idesc, kk > 0 ? 1u : 0u);
           }
+          // extra K step: ones x (-beta split) adds -W^T c to every row
+          mma_bf16(d_tmem, sw32_desc(saddr(&S.a1[0])), sw32_desc(saddr(&S.b1[bs][0])), idesc, 1u);
           mma_commit(&S.b_empty[bs]);
           mma_commit(&S.acc_full[cs]);
         }
@@ -225,19 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: 8 warps, 2 per TMEM lane quarter ----------------
+    // ---------------- epilogue: 12 warps, 3 per TMEM lane quarter ----------------
     const int e = warp - 2;
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31 are reachable by this warp
-    const int half = e >> 2;           // which half of the tile's tables
-    const int t_split = (tpt + 1) >> 1;
-    const int tl0 = half ? t_split : 0, tl1 = half ? tpt : t_split;
-    const uint32_t mask = (K >= 32) ? 0xffffffffu : ((1u << K) - 1u);
+    const int third = e >> 2;          // which third of the tile's tables
+    const int t_per = (tpt + 2) / 3;
+    const int tl0 = min(tpt, third * t_per), tl1 = min(tpt, tl0 + t_per);
+    const uint32_t mask = (1u << K) - 1u;
     uint32_t ac = 0;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
       const int u = item / mt, m0 = (item - u * mt) * kTileM;
       const int row = m0 + quarter * 32 + lane;
       const bool store = row < n0;
-      const float* bu = beta + int64_t(u) * nt * kTileN;
       bool ok = true;
       for (int n = 0; n < nt; ++n, ++ac) {
         const int cs = ac & 1;
@@ -250,28 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after();
         const int tfirst = n * tpt + tl0;
         const int tlast = min(n * tpt + tl1, L);  // exclusive
-        if (tfirst < tlast) {
+        if constexpr (KT > 0) {
+          const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(cs * kTileN);
+          if (third == 0) epi_tile_k<KT, 0>(tbase, codes, u, L, cap, row, store, n);
+          else if (third == 1) epi_tile_k<KT, 1>(tbase, codes, u, L, cap, row, store, n);
+          else epi_tile_k<KT, 2>(tbase, codes, u, L, cap, row, store, n);
+        } else if (tfirst < tlast) {
           const int c0 = tl0 * K, c1 = (tlast - n * tpt) * K;  // column range within the tile
           const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(cs * kTileN);
+          const int ch_last = (c1 - 1) >> 5;
           uint64_t buf = 0;
           int have = 0, t = tfirst;
-          for (int ch = c0 >> 5; ch * 32 < c1; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(tbase + uint32_t(ch * 32), r);
-            const float* bb = bu + n * kTileN + ch * 32;
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 b4 = __ldg(reinterpret_cast<const float4*>(bb + j));
-              // sign bit of (beta - y) is set iff y - beta > 0
-              word = __funnelshift_l(__float_as_uint(b4.x - __uint_as_float(r[j + 0])), word, 1);
-              word = __funnelshift_l(__float_as_uint(b4.y - __uint_as_float(r[j + 1])), word, 1);
-              word = __funnelshift_l(__float_as_uint(b4.z - __uint_as_float(r[j + 2])), word, 1);
-              word = __funnelshift_l(__float_as_uint(b4.w - __uint_as_float(r[j + 3])), word, 1);
-            }
-            word = __brev(word);  // bit j <-> column ch*32 + j
-            const int lo = max(c0, ch * 32);
-            const int sh = lo - ch * 32;
+          auto consume = [&](const uint32_t (&r)[32], int ch) {
+            const uint32_t word = sign_word(r);  // bit j <-> column ch*32 + j
+            const int sh = max(c0, ch * 32) - ch * 32;
             buf |= uint64_t(word >> sh) << have;
             have += 32 - sh;
             while (have >= K && t < tlast) {
@@ -280,6 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               have -= K;
               ++t;
             }
+          };
+          for (int ch = c0 >> 5; ch <= ch_last; ch += 2) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tbase + uint32_t(ch * 32), r0);
+            if (ch + 1 <= ch_last) tmem_ld32(tbase + uint32_t((ch + 1) * 32), r1);
+            tmem_wait_ld();
+            consume(r0, ch);
+            if (ch + 1 <= ch_last) consume(r1, ch + 1);
           }
         }
         fence_before();
@@ -312,31 +387,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int KT>
 cudaError_t launch_tc(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t, cudaStream_t st) {
-  CUtensorMap mk, mw;
-  if (!make_map(&mk, keys, uint64_t(g.d), uint64_t(g.units) * g.cap, kTileM)) return cudaErrorInvalidValue;
-  if (!make_map(&mw, t.wt16, uint64_t(g.d), uint64_t(g.n_w) * g.kltc, kTileN)) return cudaErrorInvalidValue;
+  CUtensorMap mk, mw, mb, mo;
+  if (!make_map(&mk, keys, uint64_t(g.d), uint64_t(g.units) * g.cap, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mw, t.wt16, uint64_t(g.d), uint64_t(g.n_w) * g.kltc, 64, kTileN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mb, t.beta, 16, uint64_t(g.units) * g.kltc, 16, kTileN, CU_TENSOR_MAP_SWIZZLE_32B) ||
+      !make_map(&mo, t.ones, 16, kTileM, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_32B))
+    return cudaErrorInvalidValue;
   const size_t smem = sizeof(GemmSmem<D>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_hash_keys_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e =
+      cudaFuncSetAttribute(k_hash_keys_tc<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   const int mt = (n_prefill + kTileM - 1) / kTileM;
   const int items = g.units * mt;
   const int grid = std::min(items, device_sm_count());
-  k_hash_keys_tc<D><<<grid, kThreads, smem, st>>>(mk, mw, t.beta, t.codes, t.hdr, g.units, g.batch * g.kvh,
-                                                  g.w_per_layer, g.cap, n_prefill, g.L, g.K, g.tpt, g.nt);
+  k_hash_keys_tc<D, KT><<<grid, kThreads, smem, st>>>(mk, mw, mb, mo, t.codes, t.hdr, g.units, g.batch * g.kvh,
+                                                  g.w_per_layer, g.cap, n_prefill, g.L, g.K, g.tpt, g.nt, g.kltc);
   return cudaGetLastError();
 }
 
@@ -346,7 +426,21 @@ cudaError_t launch_hash_keys_tc(const Geometry& g, const void* keys, int n_prefi
                                 cudaStream_t st, bool* used) {
   *used = false;
   if (g.dtype != MP_DTYPE_BF16 || g.K == 0 || n_prefill < 1 || !t.wt16) return cudaSuccess;
-  cudaError_t e = (g.d == 128) ? launch_tc<128>(g, keys, n_prefill, t, st) : launch_tc<64>(g, keys, n_prefill, t, st);
+  // K = 7..12 with d = 128 get an epilogue specialised for K; other shapes the generic one
+  cudaError_t e;
+  if (g.d == 128) {
+    switch (g.K) {
+      case 7: e = launch_tc<128, 7>(g, keys, n_prefill, t, st); break;
+      case 8: e = launch_tc<128, 8>(g, keys, n_prefill, t, st); break;
+      case 9: e = launch_tc<128, 9>(g, keys, n_prefill, t, st); break;
+      case 10: e = launch_tc<128, 10>(g, keys, n_prefill, t, st); break;
+      case 11: e = launch_tc<128, 11>(g, keys, n_prefill, t, st); break;
+      case 12: e = launch_tc<128, 12>(g, keys, n_prefill, t, st); break;
+      default: e = launch_tc<128, 0>(g, keys, n_prefill, t, st); break;
+    }
+  } else {
+    e = launch_tc<64, 0>(g, keys, n_prefill, t, st);
+  }
   if (e == cudaSuccess) *used = true;
   return e;
 }

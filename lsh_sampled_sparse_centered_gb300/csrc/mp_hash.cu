@@ -10,51 +10,38 @@
 namespace mp {
 
 // ---------------------------------------------------------------------------------
-// W [n_w][d][K*L] fp32  ->  wt32 [n_w][KLp][d] fp32 (column j = t*K + b, zero padded)
-//                       ->  wt16 [n_w][TC][d] bf16 in tensor-core column order: tile
-//                           n holds tables n*tpt .. n*tpt+tpt-1, column n*256 + i*K + b
-//                           is bit b of the tile's i-th table; the rest is zero.
+// W [n_w][d][K*L] fp32 -> wt32 [n_w][TC][d] fp32 and (bf16 configs) wt16 [n_w][TC][d]
+// in tile-aligned column order: 256-column tile n holds tables n*tpt .. n*tpt+tpt-1,
+// column n*256 + i*K + b is bit b of the tile's i-th table; the other columns are zero.
 // ---------------------------------------------------------------------------------
 __global__ void k_prepare_w(const float* __restrict__ W, float* __restrict__ wt32,
-                            __nv_bfloat16* __restrict__ wt16, int d, int K, int L, int kl, int klp, int tpt,
-                            int kltc, uint32_t* status) {
-  // tile transpose: 32 columns x 32 d-rows per block
-  __shared__ float tile[32][33];
-  const int m = blockIdx.z;
-  const int j0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int r = ty; r < 32; r += 8) {
-    const int dd = d0 + r, j = j0 + tx;
-    tile[r][tx] = (dd < d && j < kl) ? W[(int64_t(m) * d + dd) * kl + j] : 0.f;
-  }
-  __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int j = j0 + r, dd = d0 + tx;
-    if (j < klp && dd < d) wt32[(int64_t(m) * klp + j) * d + dd] = tile[tx][r];
-  }
-  if (!wt16) return;
-  // tensor-core order: this block also writes TC columns jc in [j0, j0 + 32)
+                            __nv_bfloat16* __restrict__ wt16, int d, int K, int L, int tpt, int kltc,
+                            uint32_t* status) {
+  const int m = blockIdx.y;
+  const int jc = blockIdx.x;  // one tensor-core column per block, d threads
+  const int kl = K * L;
+  const int n = jc >> 8, within = jc & 255;
+  const int i = within / K, b = within - i * K;
+  const int t = n * tpt + i;
+  const bool live = i < tpt && t < L;
   bool inexact = false;
-  for (int r = ty; r < 32; r += 8) {
-    const int jc = j0 + r, dd = d0 + tx;
-    if (jc >= kltc || dd >= d) continue;
-    const int n = jc >> 8, within = jc & 255;
-    const int i = within / K, b = within - i * K;
-    const int t = n * tpt + i;
-    float v = 0.f;
-    if (i < tpt && t < L) v = W[(int64_t(m) * d + dd) * kl + t * K + b];
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    wt16[(int64_t(m) * kltc + jc) * d + dd] = h;
-    inexact |= (__bfloat162float(h) != v);
+  for (int dd = threadIdx.x; dd < d; dd += blockDim.x) {
+    const float v = live ? W[(int64_t(m) * d + dd) * kl + t * K + b] : 0.f;
+    const int64_t o = (int64_t(m) * kltc + jc) * d + dd;
+    wt32[o] = v;
+    if (wt16) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      wt16[o] = h;
+      inexact |= (__bfloat162float(h) != v);
+    }
   }
   if (inexact) atomicOr(status, MP_STATUS_W_NOT_BF16);
 }
 
 cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st) {
-  const int cols = max(g.klp, g.kltc);
-  dim3 grid((cols + 31) / 32, (g.d + 31) / 32, g.n_w), block(32, 8);
-  k_prepare_w<<<grid, block, 0, st>>>(W, t.wt32, t.wt16, g.d, g.K, g.L, g.kl, g.klp, g.tpt, g.kltc,
-                                      &t.hdr->status);
+  if (g.kltc == 0) return cudaSuccess;
+  dim3 grid(g.kltc, g.n_w);
+  k_prepare_w<<<grid, 128, 0, st>>>(W, t.wt32, t.wt16, g.d, g.K, g.L, g.tpt, g.kltc, &t.hdr->status);
   return cudaGetLastError();
 }
 
@@ -62,29 +49,62 @@ cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs
 // centering: per unit, partial sums over `parts` token ranges, then the mean and
 // beta = W^T c. Deterministic (fixed summation order).
 // ---------------------------------------------------------------------------------
+// 16-byte loads: a row of d elements is read by d/VE lanes (VE = 8 bf16 or 4 fp32),
+// 256/(d/VE) rows per step; the partial sums of the row phases meet in shared memory.
 template <typename T>
-__global__ void k_center_parts(const T* __restrict__ keys, float* __restrict__ cparts, int d, int cap,
-                               int lo, int hi, int parts) {
-  extern __shared__ float red[];  // [blockDim.x]
+__global__ void __launch_bounds__(256) k_center_parts(const T* __restrict__ keys, float* __restrict__ cparts,
+                                                      int d, int cap, int lo, int hi, int parts) {
+  constexpr int VE = 16 / int(sizeof(T));
+  extern __shared__ float red[];  // [256 / (d / VE)][d]
   const int u = blockIdx.y, part = blockIdx.x;
+  const int lpr = d / VE, rpi = 256 / lpr;
   const int span = (hi - lo + parts - 1) / parts;
   const int t0 = lo + part * span;
   const int t1 = min(hi, t0 + span);
-  const int dim = threadIdx.x % d, phase = threadIdx.x / d, nph = blockDim.x / d;
-  const T* base = keys + int64_t(u) * cap * d;
-  float acc = 0.f;
-  for (int t = t0 + phase; t < t1; t += nph) acc += to_f(base[int64_t(t) * d + dim]);
-  red[threadIdx.x] = acc;
+  const int pl = threadIdx.x % lpr, ph = threadIdx.x / lpr;
+  const T* base = keys + int64_t(u) * cap * d + pl * VE;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int t = t0 + ph;
+  for (; t + 3 * rpi < t1; t += 4 * rpi) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = __ldg(reinterpret_cast<const uint4*>(base + int64_t(t + k * rpi) * d));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (sizeof(T) == 2) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[k]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(h[i]);
+          acc[2 * i] += f.x;
+          acc[2 * i + 1] += f.y;
+        }
+      } else {
+        acc[0] += __uint_as_float(v[k].x);
+        acc[1] += __uint_as_float(v[k].y);
+        acc[2] += __uint_as_float(v[k].z);
+        acc[3] += __uint_as_float(v[k].w);
+      }
+    }
+  }
+  for (; t < t1; t += rpi) {
+    const T* row = base + int64_t(t) * d;
+#pragma unroll
+    for (int i = 0; i < VE; ++i) acc[i] += to_f(row[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < VE; ++i) red[ph * d + pl * VE + i] = acc[i];
   __syncthreads();
-  if (phase == 0) {
-    float s = 0.f;
-    for (int p = 0; p < nph; ++p) s += red[p * d + dim];
-    cparts[(int64_t(u) * parts + part) * d + dim] = s;
+  for (int dim = threadIdx.x; dim < d; dim += blockDim.x) {
+    float sum = 0.f;
+    for (int p = 0; p < rpi; ++p) sum += red[p * d + dim];
+    cparts[(int64_t(u) * parts + part) * d + dim] = sum;
   }
 }
 
 __global__ void k_center_final(const float* __restrict__ cparts, float* __restrict__ center,
-                               float* __restrict__ beta, const __nv_bfloat16* __restrict__ wt16, int d,
+                               __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ ones,
+                               const __nv_bfloat16* __restrict__ wt16, int d,
                                int kltc, int parts, int count, int units_per_w, int64_t w_stride,
                                DevHeader* hdr, int n_prefill) {
   extern __shared__ float c[];  // [d]
@@ -97,15 +117,29 @@ __global__ void k_center_final(const float* __restrict__ cparts, float* __restri
     center[int64_t(u) * d + dim] = v;
   }
   __syncthreads();
-  // beta = W^T c in tensor-core column order (used by the tensor-core hash)
+  // -beta = -W^T c in tensor-core column order as three bf16 terms hi + mid + lo (each
+  // the bf16 rounding of what is left), an exact split of the fp32 value: the
+  // tensor-core hash adds them through one extra K step against rows of ones
   if (wt16) {
     const __nv_bfloat16* w = wt16 + int64_t(u / units_per_w) * w_stride;
     for (int j = threadIdx.x; j < kltc; j += blockDim.x) {
       const __nv_bfloat16* row = w + int64_t(j) * d;
-      float s = 0.f;
-      for (int dim = 0; dim < d; ++dim) s = fmaf(__bfloat162float(row[dim]), c[dim], s);
-      beta[int64_t(u) * kltc + j] = s;
+      float sacc = 0.f;
+      for (int dim = 0; dim < d; ++dim) sacc = fmaf(__bfloat162float(row[dim]), c[dim], sacc);
+      const float nb = -sacc;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(nb);
+      const float r1 = nb - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+      __nv_bfloat16* o = beta + (int64_t(u) * kltc + j) * 16;
+      o[0] = hi;
+      o[1] = mid;
+      o[2] = lo;
+      for (int k = 3; k < 16; ++k) o[k] = __float2bfloat16_rn(0.f);
     }
+    if (u == 0)
+      for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x)
+        ones[i] = __float2bfloat16_rn((i & 15) < 3 ? 1.f : 0.f);
   }
   if (u == 0 && threadIdx.x == 0) {
     hdr->n_prefill = n_prefill;
@@ -120,90 +154,159 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
   const int lo = min(g.s, n_prefill), hi = n_prefill;
   const int threads = 256;
   dim3 grid(g.parts, g.units);
+  // row phases per block x d floats of partial sums
   if (g.dtype == MP_DTYPE_BF16)
-    k_center_parts<__nv_bfloat16><<<grid, threads, threads * sizeof(float), st>>>(
+    k_center_parts<__nv_bfloat16><<<grid, threads, size_t(threads / (g.d / 8)) * g.d * sizeof(float), st>>>(
         static_cast<const __nv_bfloat16*>(keys), t.cparts, g.d, g.cap, lo, hi, g.parts);
   else
-    k_center_parts<float><<<grid, threads, threads * sizeof(float), st>>>(
+    k_center_parts<float><<<grid, threads, size_t(threads / (g.d / 4)) * g.d * sizeof(float), st>>>(
         static_cast<const float*>(keys), t.cparts, g.d, g.cap, lo, hi, g.parts);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
-  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.wt16, g.d,
+  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.wt16, g.d,
                                                           g.kltc, g.parts, hi - lo, g.batch * g.kvh,
                                                           w_stride, t.hdr, n_prefill);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------------
-// SimHash of rows on CUDA cores. One warp = 32 rows x one table; one thread holds
-// the K projections of its (row, table) and packs them into the code directly.
-// Rows are staged (centered, fp32) in shared memory, the block's W columns too.
+// SimHash of rows on CUDA cores: a CTA hashes R rows against one 256-column tile of
+// W (whole tables, tile-aligned order). The W tile (bf16 for bf16 configs, fp32
+// otherwise) is copied into shared memory with 16-byte loads, rows padded to an odd
+// number of words so that thread j reading column j hits distinct banks. Thread j
+// keeps the R projections of column j in registers; a warp ballot per row turns the
+// signs into bits and the bits are cut into K-bit codes.
 // ---------------------------------------------------------------------------------
-constexpr int kHashRows = 32;
-constexpr int kHashTables = 8;  // tables (warps) per block
+constexpr int kHashCols = 256;
 
-template <typename T>
-__global__ void __launch_bounds__(256) k_hash_rows(HashRowsArgs a, int d, int K, int L, int klp) {
-  extern __shared__ float sm[];
-  float* xs = sm;                              // [32][d+1]
-  float* ws = sm + kHashRows * (d + 1);        // [kHashTables*K][d]
-  const int g = blockIdx.z;
-  const int r0 = blockIdx.x * kHashRows;
-  const int t0 = blockIdx.y * kHashTables;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ void w4(const float* p, float (&w)[4]) {
+  w[0] = p[0];
+  w[1] = p[1];
+  w[2] = p[2];
+  w[3] = p[3];
+}
+__device__ __forceinline__ void w4(const __nv_bfloat16* p, float (&w)[4]) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + 2));
+  w[0] = a.x;
+  w[1] = a.y;
+  w[2] = b.x;
+  w[3] = b.y;
+}
+
+template <typename T, typename WT, int R>
+__global__ void __launch_bounds__(kHashCols) k_hash_rows(HashRowsArgs a, int d, int K, int L, int tpt, int kltc) {
+  extern __shared__ float xs[];  // [R][d] centered rows, then the W tile [256][wstride words]
+  __shared__ uint32_t bits[R][kHashCols / 32 + 1];
+  const int wstride = d * int(sizeof(WT)) / 4 + 1;  // words per W row (odd)
+  uint32_t* wsm = reinterpret_cast<uint32_t*>(xs + R * d);
+  const int g = blockIdx.z, n = blockIdx.y;
+  const int r0 = blockIdx.x * R;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (a.mark_hdr && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    if (a.mark_hdr->magic != kMagic) atomicOr(&a.mark_hdr->status, MP_STATUS_NOT_BUILT);
+    else atomicMax(&a.mark_hdr->appended_end, a.mark_pos + 1);
+  }
+  // W tile: 256 consecutive rows of d elements, one contiguous block in global memory
+  const WT* wsrc = static_cast<const WT*>(a.wt) + int64_t(g / a.groups_per_w) * a.w_stride +
+                   int64_t(n) * kHashCols * d;
+  {
+    // 8 loads in flight per thread before their shared-memory stores
+    constexpr int EPV = 16 / int(sizeof(WT));  // elements per 16-byte vector
+    constexpr int B = 8;
+    const int nvec = kHashCols * d / EPV;
+    for (int c0 = 0; c0 < nvec; c0 += B * kHashCols) {
+      uint4 v[B];
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        const int c = c0 + k * kHashCols + tid;
+        if (c < nvec) v[k] = __ldg(reinterpret_cast<const uint4*>(wsrc) + c);
+      }
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        const int c = c0 + k * kHashCols + tid;
+        if (c < nvec) {
+          const int e = c * EPV, row = e / d, wcol = (e - row * d) * int(sizeof(WT)) / 4;
+          uint32_t* dst = wsm + row * wstride + wcol;
+          dst[0] = v[k].x;
+          dst[1] = v[k].y;
+          dst[2] = v[k].z;
+          dst[3] = v[k].w;
+        }
+      }
+    }
+  }
   const T* src = static_cast<const T*>(a.src) + int64_t(g) * a.src_gs;
-  // stage rows
-  for (int i = threadIdx.x; i < kHashRows * d; i += blockDim.x) {
-    const int r = i / d, dim = i % d;
+  for (int i = tid; i < R * d; i += blockDim.x) {
+    const int r = i / d, dim = i - r * d;
     float v = 0.f;
     if (r0 + r < a.rows) {
       v = to_f(src[int64_t(a.row0 + r0 + r) * a.src_rs + dim]);
       if (a.center) v -= a.center[(int64_t(g) * a.c_gs + int64_t(r0 + r) * a.c_rs) * d + dim];
     }
-    xs[r * (d + 1) + dim] = v;
-  }
-  // stage W columns of this block's tables
-  const float* w = a.wt32 + int64_t(g / a.groups_per_w) * a.w_stride;
-  const int ncol = kHashTables * K;
-  for (int i = threadIdx.x; i < ncol * d; i += blockDim.x) {
-    const int c = i / d, dim = i % d;
-    const int j = t0 * K + c;
-    ws[i] = (j < klp) ? w[int64_t(j) * d + dim] : 0.f;
+    xs[i] = v;
   }
   __syncthreads();
-  const int t = t0 + warp;
-  const int r = r0 + lane;
-  if (t >= L || r >= a.rows) return;
-  float acc[kMaxK];
+  const WT* wrow = reinterpret_cast<const WT*>(wsm + tid * wstride);
+  float acc[R];
 #pragma unroll
-  for (int b = 0; b < kMaxK; ++b) acc[b] = 0.f;
-  const float* x = xs + lane * (d + 1);
-  const float* wc = ws + warp * K * d;
-  for (int dim = 0; dim < d; ++dim) {
-    const float xv = x[dim];
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int d0 = 0; d0 < d; d0 += 4) {
+    float w[4];
+    w4(wrow + d0, w);
 #pragma unroll
-    for (int b = 0; b < kMaxK; ++b)
-      if (b < K) acc[b] = fmaf(xv, wc[b * d + dim], acc[b]);
+    for (int r = 0; r < R; ++r) {
+      const float4 x = *reinterpret_cast<const float4*>(xs + r * d + d0);
+      acc[r] = fmaf(w[0], x.x, acc[r]);
+      acc[r] = fmaf(w[1], x.y, acc[r]);
+      acc[r] = fmaf(w[2], x.z, acc[r]);
+      acc[r] = fmaf(w[3], x.w, acc[r]);
+    }
   }
-  uint32_t code = 0;
 #pragma unroll
-  for (int b = 0; b < kMaxK; ++b)
-    if (b < K && acc[b] > 0.f) code |= 1u << b;
-  a.out[int64_t(g) * a.out_gs + int64_t(a.row0 + r) * a.out_rs + int64_t(t) * a.out_ts] = uint16_t(code);
+  for (int r = 0; r < R; ++r) {
+    const uint32_t m = __ballot_sync(0xffffffffu, acc[r] > 0.f);
+    if (lane == 0) bits[r][warp] = m;
+  }
+  if (tid < R) bits[tid][kHashCols / 32] = 0u;
+  __syncthreads();
+  const uint32_t mask = (1u << K) - 1u;
+  for (int i = tid; i < R * tpt; i += blockDim.x) {
+    const int r = i / tpt, tl = i - r * tpt;
+    const int t = n * tpt + tl;
+    if (r0 + r >= a.rows || t >= L) continue;
+    const int c0 = tl * K;
+    const uint64_t v = uint64_t(bits[r][c0 >> 5]) | (uint64_t(bits[r][(c0 >> 5) + 1]) << 32);
+    const uint32_t code = uint32_t(v >> (c0 & 31)) & mask;
+    a.out[int64_t(g) * a.out_gs + int64_t(a.row0 + r0 + r) * a.out_rs + int64_t(t) * a.out_ts] = uint16_t(code);
+  }
 }
 
+template <typename T, typename WT, int R>
+static void launch_rows_tw(const Geometry& g, const HashRowsArgs& a, cudaStream_t st) {
+  dim3 grid((a.rows + R - 1) / R, g.nt, a.groups);
+  const int wstride = g.d * int(sizeof(WT)) / 4 + 1;
+  const size_t smem = size_t(R) * g.d * sizeof(float) + size_t(kHashCols) * wstride * 4;
+  cudaFuncSetAttribute(k_hash_rows<T, WT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  k_hash_rows<T, WT, R><<<grid, kHashCols, smem, st>>>(a, g.d, g.K, g.L, g.tpt, g.kltc);
+}
+
+template <int R>
+static void launch_rows_t(const Geometry& g, const HashRowsArgs& a, cudaStream_t st) {
+  // bf16 configs hash with the bf16 copy of W (the values the tensor cores use)
+  if (g.dtype == MP_DTYPE_BF16) launch_rows_tw<__nv_bfloat16, __nv_bfloat16, R>(g, a, st);
+  else launch_rows_tw<float, float, R>(g, a, st);
+}
+
+// Row tile of 32, 16 or 8 rows: the largest that still gives two CTAs per SM.
 cudaError_t launch_hash_rows(const Geometry& g, const HashRowsArgs& a, cudaStream_t st) {
-  if (a.rows <= 0 || a.groups <= 0) return cudaSuccess;
-  dim3 grid((a.rows + kHashRows - 1) / kHashRows, (g.L + kHashTables - 1) / kHashTables, a.groups);
-  const size_t smem = (size_t(kHashRows) * (g.d + 1) + size_t(kHashTables) * g.K * g.d) * sizeof(float);
-  if (g.dtype == MP_DTYPE_BF16) {
-    cudaFuncSetAttribute(k_hash_rows<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    k_hash_rows<__nv_bfloat16><<<grid, 256, smem, st>>>(a, g.d, g.K, g.L, g.klp);
-  } else {
-    cudaFuncSetAttribute(k_hash_rows<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    k_hash_rows<float><<<grid, 256, smem, st>>>(a, g.d, g.K, g.L, g.klp);
-  }
+  if (a.rows <= 0 || a.groups <= 0 || g.nt == 0) return cudaSuccess;
+  const int64_t want = 2 * int64_t(device_sm_count());
+  auto ctas = [&](int r) { return int64_t((a.rows + r - 1) / r) * g.nt * a.groups; };
+  if (a.rows > 16 && ctas(32) >= want) launch_rows_t<32>(g, a, st);
+  else if (a.rows > 8 && ctas(16) >= want) launch_rows_t<16>(g, a, st);
+  else launch_rows_t<8>(g, a, st);
   return cudaGetLastError();
 }
 

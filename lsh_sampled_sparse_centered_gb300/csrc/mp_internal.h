@@ -13,6 +13,8 @@ constexpr uint32_t kMagic = 0x4D504947u;  // "MPIG"
 constexpr int kMaxK = 12;
 constexpr int kMaxL = 1024;
 constexpr int kMaxCapacity = 1 << 19;
+constexpr int kMaxCapacityCounters = 196608;  // bucket walk with threshold > 2: one byte per token
+constexpr int kCsrSeg = 32768;                // tokens per bucketed segment (16-bit local ids)
 constexpr int kSplitsMax = 64;
 constexpr uint32_t kExactFlag = 0x80000000u;
 
@@ -32,13 +34,14 @@ struct Geometry {
   int group;    // q_heads / kv_heads
   int units;    // layers * batch * kv_heads
   int queries;  // layers * batch * q_heads
-  int kl, klp;  // K*L and K*L rounded up to 256
+  int kl;       // K*L
   int nb;       // 2^K
   int tpt;      // tables per 256-column tensor-core tile: floor(256 / K)
   int nt;       // tensor-core column tiles: ceil(L / tpt)
   int kltc;     // nt * 256
   int match;    // MP_MATCH_CSR or MP_MATCH_SCAN (AUTO resolved)
   int cw;       // bit-plane words per table row: ceil(cap/32) rounded up to a multiple of 4
+  int nseg;     // bucketed segments per table: ceil(cap / kCsrSeg)
   int parts;    // partial sums per unit for the center
   int n_w;      // number of W matrices
 };
@@ -46,13 +49,14 @@ struct Geometry {
 struct TablesPtrs {
   DevHeader* hdr;
   float* center;
-  float* beta;
+  __nv_bfloat16* beta;   // [U][kltc][16]: -W^T c as three bf16 terms per column
+  __nv_bfloat16* ones;   // [128][16]: (1, 1, 1, 0, ...) per row
   float* wt32;
   __nv_bfloat16* wt16;
   float* cparts;
   uint16_t* codes;
-  uint32_t* off;
-  uint32_t* ids;
+  uint16_t* off;   // [U][L][nseg][nb+1]
+  uint16_t* ids;   // [U][L][cap]
   uint32_t* planes;
 };
 
@@ -76,11 +80,13 @@ struct HashRowsArgs {
   int rows, groups, row0;
   const float* center;
   int64_t c_gs, c_rs;
-  const float* wt32;      // [n_w][klp][d]
-  int64_t w_stride;       // floats between consecutive W matrices (0: shared)
+  const void* wt;         // [n_w][kltc][d], tile-aligned column order: bf16 (bf16 configs) or fp32
+  int64_t w_stride;       // elements between consecutive W matrices (0: shared)
   int groups_per_w;       // group g uses W matrix g / groups_per_w
   uint16_t* out;
   int64_t out_gs, out_rs, out_ts;
+  DevHeader* mark_hdr;    // appends: raise the appended end to mark_pos + 1 (nullptr: no-op)
+  int mark_pos;
 };
 
 // ---- launchers (each returns cudaError_t of the launch) ----

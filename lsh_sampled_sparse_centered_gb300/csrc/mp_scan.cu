@@ -55,44 +55,52 @@ cudaError_t launch_planes_append(const Geometry& g, int pos, const TablesPtrs& t
 }
 
 // Stream the planes of one KV head over 4 words (128 tokens) per thread for up to 8
-// query heads at a time; write each head's selection bitmap.
+// query heads at a time; write each head's selection bitmap. Threshold <= 2 keeps
+// the bit-sliced (ones, twos) pair; larger thresholds keep a 3-bit bit-sliced counter
+// per token and a sticky "reached" word (the count rises by at most 1 per table, so it
+// passes through the threshold exactly once).
 constexpr int kScanThreads = 128;
-constexpr int kScanHeads = 8;
 
+template <bool kGeneral>
 __global__ void __launch_bounds__(kScanThreads) k_scan(const uint32_t* __restrict__ planes,
                                                        const uint16_t* __restrict__ qcodes,
                                                        uint32_t* __restrict__ sbits, int L, int K, int cw,
                                                        int nwords, int group, int threshold) {
-  extern __shared__ uint16_t qc[];  // [group][L]
+  constexpr int H = kGeneral ? 4 : 8;  // query heads per pass
+  extern __shared__ uint16_t qc[];     // [group][L]
   const int unit = blockIdx.y;
   for (int i = threadIdx.x; i < group * L; i += blockDim.x) qc[i] = qcodes[int64_t(unit) * group * L + i];
   __syncthreads();
   const int w4 = (blockIdx.x * kScanThreads + threadIdx.x) * 4;
   if (w4 >= nwords) return;
   const uint32_t* pu = planes + int64_t(unit) * L * K * cw + w4;
-  for (int g0 = 0; g0 < group; g0 += kScanHeads) {
-    const int ng = min(kScanHeads, group - g0);
-    uint32_t ones[kScanHeads][4], twos[kScanHeads][4];
+  const uint32_t t0m = (threshold & 1) ? 0xffffffffu : 0u;
+  const uint32_t t1m = (threshold & 2) ? 0xffffffffu : 0u;
+  const uint32_t t2m = (threshold & 4) ? 0xffffffffu : 0u;
+  for (int g0 = 0; g0 < group; g0 += H) {
+    const int ng = min(H, group - g0);
+    // kGeneral: a = bit 0, b = bit 1, c = bit 2 of the count, r = reached; else a = ones, b = twos
+    uint32_t a[H][4], b[H][4], c[H][4], r[H][4];
 #pragma unroll
-    for (int g = 0; g < kScanHeads; ++g)
+    for (int g = 0; g < H; ++g)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ones[g][i] = twos[g][i] = 0u;
+      for (int i = 0; i < 4; ++i) a[g][i] = b[g][i] = c[g][i] = r[g][i] = 0u;
     for (int t = 0; t < L; ++t) {
-      uint32_t eq[kScanHeads][4];
-      uint32_t code[kScanHeads];
+      uint32_t eq[H][4];
+      uint32_t code[H];
 #pragma unroll
-      for (int g = 0; g < kScanHeads; ++g) {
+      for (int g = 0; g < H; ++g) {
         code[g] = g < ng ? qc[(g0 + g) * L + t] : 0u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) eq[g][i] = 0xffffffffu;
       }
       const uint32_t* pt = pu + int64_t(t) * K * cw;
-      for (int b = 0; b < K; ++b) {
-        const uint4 p = *reinterpret_cast<const uint4*>(pt + int64_t(b) * cw);
+      for (int bb = 0; bb < K; ++bb) {
+        const uint4 p = *reinterpret_cast<const uint4*>(pt + int64_t(bb) * cw);
 #pragma unroll
-        for (int g = 0; g < kScanHeads; ++g) {
+        for (int g = 0; g < H; ++g) {
           // (qbit ? plane : ~plane) = plane ^ (qbit - 1)
-          const uint32_t m = ((code[g] >> b) & 1u) - 1u;
+          const uint32_t m = ((code[g] >> bb) & 1u) - 1u;
           eq[g][0] &= p.x ^ m;
           eq[g][1] &= p.y ^ m;
           eq[g][2] &= p.z ^ m;
@@ -100,16 +108,26 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const uint32_t* __restric
         }
       }
 #pragma unroll
-      for (int g = 0; g < kScanHeads; ++g)
+      for (int g = 0; g < H; ++g)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          twos[g][i] |= ones[g][i] & eq[g][i];
-          ones[g][i] |= eq[g][i];
+          const uint32_t e = eq[g][i];
+          if (kGeneral) {
+            const uint32_t c0 = a[g][i] & e;  // carry into bit 1
+            a[g][i] ^= e;
+            const uint32_t c1 = b[g][i] & c0;  // carry into bit 2
+            b[g][i] ^= c0;
+            c[g][i] ^= c1;
+            r[g][i] |= ~(a[g][i] ^ t0m) & ~(b[g][i] ^ t1m) & ~(c[g][i] ^ t2m);
+          } else {
+            b[g][i] |= a[g][i] & e;
+            a[g][i] |= e;
+          }
         }
     }
     for (int g = 0; g < ng; ++g) {
       const int qh = unit * group + g0 + g;
-      const uint32_t* sel = threshold >= 2 ? twos[g] : ones[g];
+      const uint32_t* sel = kGeneral ? r[g] : (threshold >= 2 ? b[g] : a[g]);
       uint4 v;
       v.x = sel[0];
       v.y = sel[1];
@@ -127,9 +145,15 @@ cudaError_t launch_scan(const Geometry& g, int n, const TablesPtrs& t, const Dec
   if (nwords == 0) return cudaSuccess;
   dim3 grid((nwords + 4 * kScanThreads - 1) / (4 * kScanThreads), g.units);
   const size_t smem = size_t(g.group) * g.L * sizeof(uint16_t);
-  cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  k_scan<<<grid, kScanThreads, smem, st>>>(t.planes, dp.qcodes, dp.sbits, g.L, g.K, g.cw, nwords, g.group,
-                                           g.threshold);
+  if (g.threshold >= 3) {
+    cudaFuncSetAttribute(k_scan<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    k_scan<true><<<grid, kScanThreads, smem, st>>>(t.planes, dp.qcodes, dp.sbits, g.L, g.K, g.cw, nwords,
+                                                   g.group, g.threshold);
+  } else {
+    cudaFuncSetAttribute(k_scan<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    k_scan<false><<<grid, kScanThreads, smem, st>>>(t.planes, dp.qcodes, dp.sbits, g.L, g.K, g.cw, nwords,
+                                                    g.group, g.threshold);
+  }
   return cudaGetLastError();
 }
 

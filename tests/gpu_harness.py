@@ -72,14 +72,16 @@ class GpuRun:
         return v.T.copy()
 
     def unit_csr(self, u: int, tables: int):
+        """Bucketed tables of unit u for the first `tables` tables: offsets
+        [tables, NS, NB+1] and ids [tables, capacity] (16-bit, segment-local)."""
         wl = self.wl
-        nb = self.tl.n_buckets
-        o0 = self.tl.csr_offsets + u * wl.L * (nb + 1) * 4
-        i0 = self.tl.csr_ids + u * wl.L * wl.capacity * 4
-        off = self.tables[o0: o0 + tables * (nb + 1) * 4].view(torch.int32)
-        ids = self.tables[i0: i0 + tables * wl.capacity * 4].view(torch.int32)
-        return (off.cpu().numpy().astype(np.int64).reshape(tables, nb + 1),
-                ids.cpu().numpy().astype(np.int64).reshape(tables, wl.capacity))
+        nb, ns = self.tl.n_buckets, -(-wl.capacity // 32768)
+        o0 = self.tl.csr_offsets + u * wl.L * ns * (nb + 1) * 2
+        i0 = self.tl.csr_ids + u * wl.L * wl.capacity * 2
+        off = self.tables[o0: o0 + tables * ns * (nb + 1) * 2].view(torch.int16)
+        ids = self.tables[i0: i0 + tables * wl.capacity * 2].view(torch.int16)
+        return ((off.cpu().numpy().astype(np.int64) & 0xFFFF).reshape(tables, ns, nb + 1),
+                (ids.cpu().numpy().astype(np.int64) & 0xFFFF).reshape(tables, wl.capacity))
 
     def unit_planes(self, u: int, tables: int) -> np.ndarray:
         """Bit-planes of unit u for the first `tables` tables, [tables, K, CW] as int64."""
@@ -153,15 +155,24 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
 
 
-def check_csr(off: np.ndarray, ids: np.ndarray, codes: np.ndarray, lo: int, hi: int, nb: int) -> None:
-    """CSR of one table against the (GPU) codes it was built from: bucket b holds
-    exactly the tokens of [lo, hi) with code b, ascending."""
-    c = codes[lo:hi]
-    counts = np.bincount(c, minlength=nb)
-    assert off[0] == 0 and off[nb] == hi - lo
-    np.testing.assert_array_equal(np.diff(off), counts)
-    order = np.argsort(c, kind="stable") + lo
-    np.testing.assert_array_equal(ids[: hi - lo], order)
+def check_csr(off: np.ndarray, ids: np.ndarray, codes: np.ndarray, lo: int, hi: int, nb: int,
+              seg: int = 32768) -> None:
+    """Bucketed segments of one table against the (GPU) codes they were built from:
+    in segment s (tokens [lo + s*seg, ...)), bucket b holds exactly the tokens with
+    code b, stored as offsets from the segment's first token. The order inside a
+    bucket is not unique (the build places tokens with shared-memory atomics), so
+    the check is: the ids of a segment are a permutation of its tokens and the codes
+    they point at, read in id order, are the bucket numbers the offsets give."""
+    for si, a in enumerate(range(lo, hi, seg)):
+        b = min(hi, a + seg)
+        c = codes[a:b]
+        o = off[si]
+        counts = np.bincount(c, minlength=nb)
+        assert o[0] == 0 and o[nb] == b - a
+        np.testing.assert_array_equal(np.diff(o), counts)
+        got = ids[si * seg: si * seg + (b - a)]
+        np.testing.assert_array_equal(np.sort(got), np.arange(b - a))
+        np.testing.assert_array_equal(c[got], np.repeat(np.arange(nb), counts))
 
 
 # ----------------------------------------------------------------------------------

@@ -47,11 +47,14 @@ def _cfg(mp, **kw):
 
 def test_config_validation(mp):
     assert mp.mp_config_check(_cfg(mp)) == mp.MP_OK
+    assert mp.mp_config_check(_cfg(mp, threshold=3)) == mp.MP_OK
+    assert mp.mp_config_check(_cfg(mp, threshold=7, capacity=200000, match_mode=2)) == mp.MP_OK
     bad = [dict(q_heads=3), dict(layers=0), dict(K=-1), dict(L=0), dict(capacity=0), dict(dtype=7),
            dict(threshold=0), dict(window=-1), dict(match_mode=9)]
     for b in bad:
         assert mp.mp_config_check(_cfg(mp, **b)) == mp.MP_ERR_INVALID_ARG, b
-    unsup = [dict(head_dim=96), dict(K=13), dict(L=2000), dict(capacity=(1 << 19) + 1), dict(threshold=3)]
+    unsup = [dict(head_dim=96), dict(K=13), dict(L=2000), dict(capacity=(1 << 19) + 1), dict(threshold=8),
+             dict(threshold=3, L=300), dict(threshold=3, capacity=200000, match_mode=1)]
     for u in unsup:
         assert mp.mp_config_check(_cfg(mp, **u)) == mp.MP_ERR_UNSUPPORTED, u
     c = _cfg(mp)
@@ -62,14 +65,15 @@ def test_config_validation(mp):
 def test_layouts_are_aligned_disjoint_and_sized(mp):
     c = _cfg(mp, layers=2, w_per_layer=True)
     t = mp.mp_tables_layout_get(c)
-    names = ["header", "center", "beta", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets", "csr_ids"]
+    names = ["header", "center", "beta", "ones", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets",
+             "csr_ids"]
     offs = [getattr(t, n) for n in names]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and len(set(offs)) == len(offs)
     U, L, cap, d = 2 * 1 * 2, 75, 4096, 128
     assert t.csr_offsets - t.codes >= U * L * cap * 2
-    assert t.total_bytes - t.csr_ids >= U * L * cap * 4
-    assert t.kl_padded == 768 and t.n_buckets == 256
+    assert t.total_bytes - t.csr_ids >= U * L * cap * 2
+    assert t.tc_cols == 768 and t.n_buckets == 256
     assert t.wt_bf16 - t.wt_f32 >= 2 * 768 * d * 4
     dl = mp.mp_decode_layout_get(c)
     Q = 2 * 4

@@ -67,11 +67,16 @@ def test_dtypes_and_head_dims(mp, kw):
     _report(str(kw), rep)
 
 
-def test_threshold_one(mp):
-    wl = WL.Workload("t1", layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=128, n_prefill=3000, steps=1,
-                     append=False, K=10, L=12, dtype="bf16", seed=31)
-    rep = check_workload(mp, wl, WL.generate(wl), threshold=1)
-    _report("threshold1", rep)
+@pytest.mark.parametrize("threshold,mode", [(1, 1), (1, 2), (3, 1), (3, 2), (5, 1), (7, 2)])
+def test_thresholds(mp, threshold, mode):
+    """u = P[Bin(L, p^K) >= T] and the sampling rule for T other than the pages' 2
+    (a reviewer's question in the authors' responses), in both match modes."""
+    wl = WL.Workload(f"t{threshold}", layers=1, batch=1, kv_heads=2, q_heads=4, head_dim=128, n_prefill=3000,
+                     steps=20, append=True, K=6, L=40, dtype="bf16", seed=31 + threshold, window=8)
+    rep = check_workload(mp, wl, WL.generate(wl), threshold=threshold, match_mode=mode, steps=[0, 19],
+                         check_csr_tables=wl.L)
+    _report(f"threshold {threshold}", rep)
+    assert rep["match_mode"] == mode
 
 
 def test_K0_samples_everything_and_equals_exact_attention(mp):
