@@ -108,6 +108,8 @@ typedef struct mp_tables_layout {
                             the rest zero), tile-aligned column order; with `ones` it is the
                             extra K step of the tensor-core projection that subtracts W^T·center */
   uint64_t ones;         /* bf16 [128][16]: rows of (1, 1, 1, 0, ..., 0) */
+  uint64_t negbeta_f32;  /* float [U][TC]: -W^T·center in tile-aligned column order (centering of
+                            appended keys hashed on the tensor cores) */
   uint64_t wt_f32;       /* float [layers or 1][TC][d]: W transposed, tile-aligned column order */
   uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: the same in bf16 (bf16 configs only, else 0) */
   uint64_t center_parts; /* float [U][parts][d]: partial sums while building */

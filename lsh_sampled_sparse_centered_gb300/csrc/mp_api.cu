@@ -101,6 +101,8 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
   off = align256(off + U * uint64_t(g.kltc) * 16 * 2);
   o->ones = off;
   off = align256(off + 128 * 16 * 2);
+  o->negbeta_f32 = off;
+  off = align256(off + U * uint64_t(g.kltc) * 4);
   o->wt_f32 = off;
   off = align256(off + uint64_t(g.n_w) * g.kltc * d * 4);
   if (g.dtype == MP_DTYPE_BF16) {
@@ -161,6 +163,7 @@ static TablesPtrs tables_ptrs(const Geometry& g, void* base) {
   t.center = reinterpret_cast<float*>(b + l.center);
   t.beta = reinterpret_cast<__nv_bfloat16*>(b + l.beta);
   t.ones = reinterpret_cast<__nv_bfloat16*>(b + l.ones);
+  t.negbeta = reinterpret_cast<float*>(b + l.negbeta_f32);
   t.wt32 = reinterpret_cast<float*>(b + l.wt_f32);
   t.wt16 = l.wt_bf16 ? reinterpret_cast<__nv_bfloat16*>(b + l.wt_bf16) : nullptr;
   t.cparts = reinterpret_cast<float*>(b + l.center_parts);
@@ -208,10 +211,17 @@ int device_sm_count() {
   return cache[dev];
 }
 
-// Hash path for bf16 keys at build time: tensor cores unless MP_HASH_PATH=simt.
+// Hash path for bf16 keys, queries and appends: tensor cores unless MP_HASH_PATH=simt.
 static bool use_simt_hash() {
   const char* e = std::getenv("MP_HASH_PATH");
   return e && std::strcmp(e, "simt") == 0;
+}
+
+// Decode-time rows (queries, appended keys) go through the swap-AB tensor-core kernel
+// for bf16 with d = 64 or 128.
+static bool rows_on_tensor_cores(const Geometry& g, const TablesPtrs& t) {
+  return g.dtype == MP_DTYPE_BF16 && (g.d == 64 || g.d == 128) && g.K > 0 && g.nt > 0 && t.wt16 &&
+         !use_simt_hash();
 }
 
 // Number of slices per query head for the attention: about 256 list entries per
@@ -424,7 +434,25 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   // then a one-thread kernel does it)
   a.mark_hdr = g.nt > 0 ? t.hdr : nullptr;
   a.mark_pos = pos;
-  {
+  if (rows_on_tensor_cores(g, t)) {
+    RowsHashTc h;
+    std::memset(&h, 0, sizeof(h));
+    h.x = static_cast<const __nv_bfloat16*>(keys) + int64_t(pos) * g.d;
+    h.x_rs = int64_t(g.cap) * g.d;
+    h.rows = g.batch * g.kvh;
+    h.groups = g.layers;
+    h.groups_per_w = 1;
+    h.wt16 = t.wt16;
+    h.negbeta = t.negbeta;
+    h.out = t.codes + pos;
+    h.out_gs = a.out_gs;
+    h.out_rs = a.out_rs;
+    h.out_ts = a.out_ts;
+    h.hdr = t.hdr;
+    h.mark_pos = pos;
+    ProfScope ps(st, K_HASH_APPEND);
+    if (launch_hash_rows_tc(g, h, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
     ProfScope ps(st, K_HASH_APPEND);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
   }
@@ -478,6 +506,23 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   if (g.K == 0) {
     if (cudaMemsetAsync(dp.qcodes, 0, size_t(g.queries) * g.L * sizeof(uint16_t), st) != cudaSuccess)
       return MP_ERR_CUDA;
+  } else if (rows_on_tensor_cores(g, t)) {
+    RowsHashTc h;
+    std::memset(&h, 0, sizeof(h));
+    h.x = static_cast<const __nv_bfloat16*>(q);
+    h.x_rs = g.d;
+    h.rows = g.batch * g.qh;
+    h.groups = g.layers;
+    h.groups_per_w = 1;
+    h.wt16 = t.wt16;
+    h.negbeta = nullptr;
+    h.out = dp.qcodes;
+    h.out_gs = a.out_gs;
+    h.out_rs = a.out_rs;
+    h.out_ts = a.out_ts;
+    h.hdr = t.hdr;
+    ProfScope ps(st, K_HASH_QUERY);
+    if (launch_hash_rows_tc(g, h, st) != cudaSuccess) return MP_ERR_CUDA;
   } else {
     ProfScope ps(st, K_HASH_QUERY);
     if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;

@@ -20,7 +20,10 @@ namespace mp {
 // bucket, `seen2` in >= 2. With threshold 2 the sampled set is seen2 restricted to
 // [n_sink, n - window); with threshold 1 it is seen1. Compaction writes S in
 // ascending token order, then the exact tokens (bit 31 set).
-__global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
+constexpr int kMatchWarps = 8;
+
+template <int PER>
+__global__ void __launch_bounds__(kMatchWarps * 32, 4) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
                                                    const uint16_t* __restrict__ off,
@@ -28,7 +31,7 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
                                                    int32_t* __restrict__ list_len, int32_t* __restrict__ sample_count,
                                                    uint32_t* __restrict__ counters, int n, int s, int w, int L,
                                                    int nb, int cap, int nseg, int group, int threshold) {
-  extern __shared__ uint32_t sm[];
+  extern __shared__ __align__(16) uint32_t sm[];
   const int qh = blockIdx.x;
   const int unit = qh / group;  // [layer][batch][q_head] -> [layer][batch][kv_head]
   const int lo = min(s, n);
@@ -41,10 +44,8 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
   uint32_t* seen2 = sm + nwords;
   uint32_t* cnt = sm + nwords;  // [nwords * 8] byte counters (threshold >= 3)
   const int body = bytes ? nwords * 9 : nwords * 2;
-  uint32_t* bstart = sm + body;          // [L * nseg]: bucket start in the unit's id arrays
-  uint32_t* bsize = bstart + L * nseg;   // [L * nseg + 1]: sizes, then their exclusive scan
-  uint16_t* qc = reinterpret_cast<uint16_t*>(bsize + L * nseg + 1);
-  __shared__ uint32_t wtot[8];
+  uint2* bkt = reinterpret_cast<uint2*>(sm + ((body + 1) & ~1));  // [L * nseg] bucket ranges
+  uint16_t* qc = reinterpret_cast<uint16_t*>(bkt + L * nseg);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   const bool built = hdr->magic == kMagic;
@@ -55,16 +56,15 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
     if (!built) atomicOr(&hdr->status, MP_STATUS_NOT_BUILT);
     else if (hi > app_end) atomicOr(&hdr->status, MP_STATUS_APPEND_GAP);
   }
-  for (int i = threadIdx.x; i < body; i += blockDim.x) sm[i] = 0u;
+  for (int i = threadIdx.x; i < (body >> 2); i += blockDim.x) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = (body & ~3) + threadIdx.x; i < body; i += blockDim.x) sm[i] = 0u;
   for (int t = threadIdx.x; t < L; t += blockDim.x) qc[t] = qcodes[int64_t(qh) * L + t];
   __syncthreads();
 
   if (built && hi > lo) {
     // tokens hashed at build time: the query's bucket in every (table, segment). The
-    // bucket ranges are fetched first (one round trip for all of them), then a block
-    // scan of their sizes numbers all bucket entries 0 .. total-1, and the threads walk
-    // that flat range 8 entries at a time (8 independent id loads in flight each),
-    // finding an entry's bucket by binary search over the scanned sizes.
+    // bucket ranges are fetched first (one round trip for all of them); then each warp
+    // takes TB buckets at a time (buckets average 32768 / 2^K entries) and marks them.
     const int64_t tbase = int64_t(unit) * L;
     const int lo_b = min(s, n0);  // first token bucketed at build time
     const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
@@ -74,66 +74,81 @@ __global__ void __launch_bounds__(256) k_match_csr(DevHeader* hdr,
       const uint16_t* o = off + ((tbase + t) * nseg + sg) * (nb + 1);
       const int code = qc[t];
       const uint32_t b0 = __ldg(&o[code]), b1 = __ldg(&o[code + 1]);
-      // absolute position of the bucket in the table's id array
-      bstart[p] = uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0;
-      bsize[p] = b1 - b0;
+      // {position of the bucket in the unit's id arrays, size | segment << 16}
+      bkt[p] = make_uint2(uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0, (b1 - b0) | (uint32_t(sg) << 16));
     }
     __syncthreads();
-    // exclusive scan of bsize in place (thread i owns pairs [i*per, (i+1)*per))
-    {
-      const int per = (pairs + blockDim.x - 1) / blockDim.x;
-      const int p0 = min(pairs, int(threadIdx.x) * per), p1 = min(pairs, p0 + per);
-      uint32_t local = 0;
-      for (int p = p0; p < p1; ++p) local += bsize[p];
-      uint32_t x = local;
-#pragma unroll
-      for (int k = 1; k < 32; k <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, k);
-        if (lane >= k) x += y;
-      }
-      if (lane == 31) wtot[warp] = x;
-      __syncthreads();
-      uint32_t run = x - local;
-      for (int k = 0; k < warp; ++k) run += wtot[k];
-      for (int p = p0; p < p1; ++p) {
-        const uint32_t v = bsize[p];
-        bsize[p] = run;
-        run += v;
-      }
-      if (threadIdx.x == blockDim.x - 1) bsize[pairs] = run;
-    }
-    __syncthreads();
-    const uint32_t total = bsize[pairs];
     const uint16_t* idu = ids + tbase * cap;
-    constexpr int kIn = 8;
-    for (uint32_t f0 = threadIdx.x; f0 < total; f0 += kIn * blockDim.x) {
-      uint32_t tk[kIn];
-#pragma unroll
-      for (int j = 0; j < kIn; ++j) {
-        const uint32_t f = f0 + j * blockDim.x;
-        tk[j] = 0xffffffffu;
-        if (f < total) {
-          // last pair whose first entry is <= f
-          int l = 0, r = pairs - 1;
-          while (l < r) {
-            const int mid = (l + r + 1) >> 1;
-            if (bsize[mid] <= f) l = mid;
-            else r = mid - 1;
-          }
-          const uint32_t sg = (l - (l / nsu) * nsu);
-          tk[j] = uint32_t(lo_b) + sg * kCsrSeg + __ldg(&idu[bstart[l] + (f - bsize[l])]);
+    auto mark = [&](uint32_t tok) {
+      if (tok < uint32_t(hi)) {
+        if (bytes) {
+          atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
+        } else {
+          const uint32_t bit = 1u << (tok & 31);
+          const uint32_t old = atomicOr(&seen1[tok >> 5], bit);
+          if (old & bit) atomicOr(&seen2[tok >> 5], bit);
         }
       }
+    };
+    // lane i loads entries i, i + 32, ... (PER of them) of each of TB buckets: 32 loads
+    // in flight per lane. All first marks of a batch are issued before the second ones,
+    // so that the atomics do not wait on one another. The rare bucket above 32 * PER
+    // entries finishes in a second loop, 4 loads per lane at a time.
+    constexpr int TB = 32 / PER;
+    for (int p0 = warp * TB; p0 < pairs; p0 += kMatchWarps * TB) {
+      uint32_t tk[TB][PER];
+      bool big = false;
 #pragma unroll
-      for (int j = 0; j < kIn; ++j) {
-        const uint32_t tok = tk[j];
-        if (tok < uint32_t(hi)) {
-          if (bytes) {
-            atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
-          } else {
-            const uint32_t bit = 1u << (tok & 31);
-            const uint32_t old = atomicOr(&seen1[tok >> 5], bit);
-            if (old & bit) atomicOr(&seen2[tok >> 5], bit);
+      for (int j = 0; j < TB; ++j) {
+        const bool live = p0 + j < pairs;
+        const uint2 e = live ? bkt[p0 + j] : make_uint2(0u, 0u);
+        const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
+        big |= sz > 32u * PER;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          const uint32_t i = 32u * k + lane;
+          tk[j][k] = i < sz ? tok0 + __ldg(&idu[e.x + i]) : 0xffffffffu;
+        }
+      }
+      if (bytes) {
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+#pragma unroll
+          for (int k = 0; k < PER; ++k) {
+            const uint32_t tok = tk[j][k];
+            if (tok < uint32_t(hi)) atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
+          }
+      } else {
+        uint64_t dup = 0;
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+#pragma unroll
+          for (int k = 0; k < PER; ++k) {
+            const uint32_t tok = tk[j][k];
+            if (tok < uint32_t(hi)) {
+              const uint32_t bit = 1u << (tok & 31);
+              if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1ull << (j * PER + k);
+            }
+          }
+#pragma unroll
+        for (int j = 0; j < TB; ++j)
+#pragma unroll
+          for (int k = 0; k < PER; ++k)
+            if ((dup >> (j * PER + k)) & 1ull) atomicOr(&seen2[tk[j][k] >> 5], 1u << (tk[j][k] & 31));
+      }
+      if (__any_sync(0xffffffffu, big)) {
+        for (int j = 0; j < TB && p0 + j < pairs; ++j) {
+          const uint2 e = bkt[p0 + j];
+          const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
+          for (uint32_t i0 = 32u * PER; i0 < sz; i0 += 128u) {
+            uint32_t t4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t i = i0 + 32u * k + lane;
+              t4[k] = i < sz ? tok0 + __ldg(&idu[e.x + i]) : 0xffffffffu;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mark(t4[k]);
           }
         }
       }
@@ -183,11 +198,18 @@ cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, cons
   const int hi = max(lo, n - g.w);
   const int nwords = (hi + 31) >> 5;
   const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
-  const size_t smem = size_t(body) * 4 + size_t(g.L) * g.nseg * 8 + 4 + size_t(g.L) * 2 + 16;
-  cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  k_match_csr<<<g.queries, 256, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists, dp.list_len,
-                                            dp.sample_count, dp.counters, n, g.s, g.w, g.L, g.nb, g.cap,
-                                            g.nseg, g.group, g.threshold);
+  const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 8 + size_t(g.L) * 2 + 16;
+  // entries per lane and bucket from the mean bucket size of a segment
+  const int mean = std::min(kCsrSeg, n) >> g.K;
+  auto go = [&](auto kern) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    kern<<<g.queries, kMatchWarps * 32, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists, dp.list_len,
+                                                    dp.sample_count, dp.counters, n, g.s, g.w, g.L, g.nb, g.cap,
+                                                    g.nseg, g.group, g.threshold);
+  };
+  if (mean <= 24) go(k_match_csr<1>);
+  else if (mean <= 48) go(k_match_csr<2>);
+  else go(k_match_csr<4>);
   return cudaGetLastError();
 }
 
@@ -253,20 +275,16 @@ constexpr int kAttThreads = 128;
 constexpr int kGatherUnroll = 8;
 constexpr int kListChunk = 1024;
 
-__device__ __forceinline__ void unpack8(const uint4& v, const __nv_bfloat16*, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 x = __bfloat1622float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
-  }
+// a 16-byte slice of a row as packed fp32 pairs: 4 pairs of bf16, or 2 pairs of fp32
+__device__ __forceinline__ void pairs_of(const uint4& v, const __nv_bfloat16*, uint64_t (&f)[4]) {
+  f[0] = bf2_to_f2(v.x);
+  f[1] = bf2_to_f2(v.y);
+  f[2] = bf2_to_f2(v.z);
+  f[3] = bf2_to_f2(v.w);
 }
-__device__ __forceinline__ void unpack8(const uint4& v, const float*, float (&f)[4]) {
-  f[0] = __uint_as_float(v.x);
-  f[1] = __uint_as_float(v.y);
-  f[2] = __uint_as_float(v.z);
-  f[3] = __uint_as_float(v.w);
+__device__ __forceinline__ void pairs_of(const uint4& v, const float*, uint64_t (&f)[2]) {
+  f[0] = (uint64_t(v.y) << 32) | v.x;
+  f[1] = (uint64_t(v.w) << 32) | v.z;
 }
 
 // Transposed butterfly over the LPR lanes of a row set: on entry s[u] is this lane's
@@ -300,7 +318,7 @@ __device__ __forceinline__ int row_lane(int sub, int u) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
+__global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_gather(
     const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
     const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
     float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
@@ -329,17 +347,19 @@ __global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
   const T* kbase = keys + int64_t(unit) * cap * D + part * VE;
   const T* vbase = values + int64_t(unit) * cap * D + part * VE;
 
-  float qr[VE], cr[VE];
-#pragma unroll
-  for (int i = 0; i < VE; ++i) {
-    qr[i] = to_f(q[int64_t(qh) * D + part * VE + i]);
-    cr[i] = center[int64_t(unit) * D + part * VE + i];
-  }
+  constexpr int NP = VE / 2;  // packed pairs per slice
+  uint64_t q2[NP], c2[NP];
   float qq = 0.f, qc = 0.f;
 #pragma unroll
-  for (int i = 0; i < VE; ++i) {
-    qq = fmaf(qr[i], qr[i], qq);
-    qc = fmaf(qr[i], cr[i], qc);
+  for (int i = 0; i < NP; ++i) {
+    const float q0 = to_f(q[int64_t(qh) * D + part * VE + 2 * i]);
+    const float q1 = to_f(q[int64_t(qh) * D + part * VE + 2 * i + 1]);
+    const float c0 = center[int64_t(unit) * D + part * VE + 2 * i];
+    const float c1 = center[int64_t(unit) * D + part * VE + 2 * i + 1];
+    q2[i] = pk2(q0, q1);
+    c2[i] = pk2(c0, c1);
+    qq = fmaf(q0, q0, fmaf(q1, q1, qq));
+    qc = fmaf(q0, c0, fmaf(q1, c1, qc));
   }
 #pragma unroll
   for (int o = LPR / 2; o >= 1; o >>= 1) {
@@ -352,9 +372,9 @@ __global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
   const float scale = rsqrtf(float(D));
 
   float m_run = -CUDART_INF_F, l_run = 0.f;
-  float acc[VE];
+  uint64_t acc2[NP];
 #pragma unroll
-  for (int i = 0; i < VE; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NP; ++i) acc2[i] = 0ull;
 
   // the slice's list entries go through shared memory (one round trip per chunk), so
   // that each group only waits for its K and V rows
@@ -388,17 +408,17 @@ __global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
     float sa[U], sn[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      float kf[VE];
-      unpack8(kv[u], static_cast<const T*>(nullptr), kf);
-      float a = 0.f, c = 0.f;
+      uint64_t k2[NP];
+      pairs_of(kv[u], static_cast<const T*>(nullptr), k2);
+      uint64_t a2 = 0ull, n2 = 0ull;
 #pragma unroll
-      for (int i = 0; i < VE; ++i) {
-        const float c0 = kf[i] - cr[i];
-        a = fmaf(qr[i], kf[i], a);
-        c = fmaf(c0, c0, c);
+      for (int i = 0; i < NP; ++i) {
+        const uint64_t d2 = sub2(k2[i], c2[i]);
+        a2 = fma2(q2[i], k2[i], a2);
+        n2 = fma2(d2, d2, n2);
       }
-      sa[u] = a;
-      sn[u] = c;
+      sa[u] = lo2(a2) + hi2(a2);
+      sn[u] = lo2(n2) + hi2(n2);
     }
     const float rd = reduce_rows8<LPR>(sa, lane);
     const float rkk = reduce_rows8<LPR>(sn, lane);
@@ -433,16 +453,18 @@ __global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
     // each lane's weights for its rows: the row lane's logit, shifted by the new maximum
     const float pw = (lg == -CUDART_INF_F) ? 0.f : __expf(lg - m_new);
     float ps = 0.f;
+    const uint64_t al2 = pk2(alpha, alpha);
 #pragma unroll
-    for (int i = 0; i < VE; ++i) acc[i] *= alpha;
+    for (int i = 0; i < NP; ++i) acc2[i] = mul2(acc2[i], al2);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float p = __shfl_sync(0xffffffffu, pw, row_lane<LPR>(sub, u));
       ps += p;
-      float vf[VE];
-      unpack8(vv[u], static_cast<const T*>(nullptr), vf);
+      const uint64_t p2 = pk2(p, p);
+      uint64_t v2[NP];
+      pairs_of(vv[u], static_cast<const T*>(nullptr), v2);
 #pragma unroll
-      for (int i = 0; i < VE; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
+      for (int i = 0; i < NP; ++i) acc2[i] = fma2(p2, v2[i], acc2[i]);
     }
 #pragma unroll
     for (int o = LPR; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
@@ -450,6 +472,12 @@ __global__ void __launch_bounds__(kAttThreads, 4) k_attend_gather(
     m_run = m_new;
   }
   __syncthreads();  // before the next chunk overwrites the staged entries
+  }
+  float acc[VE];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    acc[2 * i] = lo2(acc2[i]);
+    acc[2 * i + 1] = hi2(acc2[i]);
   }
   // rows of the other sub-groups of lanes hold the same dims: fold them
 #pragma unroll

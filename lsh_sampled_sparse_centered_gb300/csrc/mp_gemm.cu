@@ -374,6 +374,166 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && S.abort) atomicOr(&hdr->status, MP_STATUS_WAIT_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------------
+// SimHash of a few rows per W matrix (decode queries, appended keys) on the tensor
+// cores, with the roles of the operands swapped: A = 256 W columns (two M = 128
+// halves), B = up to 256 rows (N), so that a tensor-memory lane is a W column and a
+// ballot across a warp's lanes gives one row's sign bits of 32 columns at once.
+// One CTA per (W group, 256-column tile, row block): thread 0 issues the TMA loads and
+// the MMAs, then all 8 warps read the accumulator (warp w: half w / 4, lanes of
+// quarter w % 4), add -beta for appended keys, ballot the signs into a shared
+// [row][32-column block] bitmap, and cut the codes.
+// ---------------------------------------------------------------------------------
+constexpr int kRowsWarps = 8;
+
+template <int D>
+struct RowsLayout {
+  static constexpr int kSub = D / 64;
+  static constexpr uint32_t kABytes = 256u * 64u * 2u;  // one 64-element slab of 256 W columns
+  __host__ __device__ static constexpr uint32_t a_off(int s) { return uint32_t(s) * kABytes; }
+  __host__ __device__ static constexpr uint32_t b_off(int s, int nr) {
+    return uint32_t(kSub) * kABytes + uint32_t(s) * uint32_t(nr) * 128u;
+  }
+  __host__ __device__ static constexpr uint32_t bits_off(int nr) { return b_off(kSub, nr); }
+  __host__ __device__ static constexpr uint32_t ctl_off(int nr) { return bits_off(nr) + uint32_t(nr) * 9u * 4u; }
+  __host__ __device__ static constexpr uint32_t bytes(int nr) { return ctl_off(nr) + 64u; }
+};
+
+struct RowsTcArgs {
+  int rows;          // rows per group
+  int nr;            // rows per CTA (multiple of 32, <= 256)
+  int groups_per_w;  // group g uses W matrix g / groups_per_w
+  int w_rows;        // W rows between consecutive W matrices (0: shared)
+  const float* negbeta;  // appended keys: -beta [U][kltc] (nullptr: queries)
+  int kltc;
+  uint16_t* out;
+  int64_t out_gs, out_rs, out_ts;
+  DevHeader* hdr;    // status word; appends also raise the appended end to mark_pos + 1
+  int mark_pos;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kRowsWarps * 32)
+    k_hash_rows_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, RowsTcArgs a,
+                   int L, int K, int tpt) {
+  using Lay = RowsLayout<D>;
+  constexpr int kSub = Lay::kSub;
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  const uint32_t sbase = saddr(smraw);
+  unsigned char* sm = smraw + ((1024 - (sbase & 1023)) & 1023);
+  const int nr = a.nr;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(sm + Lay::bits_off(nr));  // [nr][9]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::ctl_off(nr));
+  uint64_t* accb = full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile uint32_t* abort = tmem_slot + 1;
+  const int g = blockIdx.z, n = blockIdx.y, rb = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = rb * nr;                   // first row of this CTA within its group
+  const int nvalid = min(nr, a.rows - r0);  // rows stored
+  uint32_t ncols = 32;
+  while (ncols < uint32_t(2 * nr)) ncols <<= 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(full, 1);
+    mbar_init(accb, 1);
+    *abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (a.negbeta && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+      if (a.hdr->magic != kMagic) atomicOr(&a.hdr->status, MP_STATUS_NOT_BUILT);
+      else atomicMax(&a.hdr->appended_end, a.mark_pos + 1);
+    }
+  }
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) bits[i * 9 + 8] = 0u;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    const int wrow = (g / a.groups_per_w) * a.w_rows + n * 256;
+    const int xrow = g * a.rows + r0;
+    mbar_expect_tx(full, uint32_t(kSub) * (Lay::kABytes + uint32_t(nr) * 128u));
+    for (int s = 0; s < kSub; ++s) {
+      tma_load_2d(sm + Lay::a_off(s), &tmW, s * 64, wrow, full);
+      tma_load_2d(sm + Lay::b_off(s, nr), &tmX, s * 64, xrow, full);
+    }
+    if (mbar_wait(full, 0, abort)) {
+      fence_after();
+      // D[col][row]: M = 128 W columns per half, N = nr rows
+      const uint32_t idesc =
+          (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nr >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int s = kk >> 2, off = (kk & 3) * 32;
+          const uint64_t da = sw128_desc(saddr(sm + Lay::a_off(s)) + uint32_t(h) * 16384u + off);
+          const uint64_t db = sw128_desc(saddr(sm + Lay::b_off(s, nr)) + off);
+          mma_bf16(tmem + uint32_t(h * nr), da, db, idesc, kk > 0 ? 1u : 0u);
+        }
+      mma_commit(accb);
+    }
+  }
+  __syncwarp();
+  // epilogue: all warps. -beta of the first 32 rows is fetched before the wait for the
+  // accumulator (it does not depend on it)
+  const int h = warp >> 2, quarter = warp & 3;
+  const int col = h * 128 + quarter * 32 + lane;  // column within the 256-column tile
+  const float* nbc =
+      a.negbeta ? a.negbeta + (int64_t(g) * a.rows + r0) * a.kltc + int64_t(n) * 256 + col : nullptr;
+  float nb[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) nb[j] = (nbc && j < nvalid) ? __ldg(nbc + int64_t(j) * a.kltc) : 0.f;
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort));
+  if (ok) {
+    fence_after();
+    for (int ch = 0; ch < (nvalid + 31) / 32; ++ch) {
+      if (ch > 0)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          nb[j] = (nbc && ch * 32 + j < nvalid) ? __ldg(nbc + int64_t(ch * 32 + j) * a.kltc) : 0.f;
+      uint32_t r[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * nr + ch * 32), r);
+      tmem_wait_ld();
+      uint32_t mine = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t w = __ballot_sync(0xffffffffu, __uint_as_float(r[j]) + nb[j] > 0.f);
+        if (lane == j) mine = w;
+      }
+      const int row = ch * 32 + lane;
+      if (row < nr) bits[row * 9 + h * 4 + quarter] = mine;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  }
+  if (*abort) {
+    if (threadIdx.x == 0) atomicOr(&a.hdr->status, MP_STATUS_WAIT_TIMEOUT);
+    return;
+  }
+  const uint32_t mask = (1u << K) - 1u;
+  for (int i = threadIdx.x; i < nvalid * tpt; i += blockDim.x) {
+    const int row = i / tpt, tl = i - row * tpt;
+    const int t = n * tpt + tl;
+    if (t >= L) continue;
+    const int c0 = tl * K;
+    const uint64_t v = uint64_t(bits[row * 9 + (c0 >> 5)]) | (uint64_t(bits[row * 9 + (c0 >> 5) + 1]) << 32);
+    a.out[int64_t(g) * a.out_gs + int64_t(r0 + row) * a.out_rs + int64_t(t) * a.out_ts] =
+        uint16_t(uint32_t(v >> (c0 & 31)) & mask);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -393,6 +553,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// rows `row_bytes` apart (a multiple of 16)
+bool make_map_strided(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -420,7 +594,40 @@ cudaError_t launch_tc(const Geometry& g, const void* keys, int n_prefill, const 
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st) {
+  RowsTcArgs a;
+  a.rows = h.rows;
+  a.nr = std::min(256, (h.rows + 31) / 32 * 32);
+  a.groups_per_w = h.groups_per_w;
+  a.w_rows = g.w_per_layer ? g.kltc : 0;
+  a.negbeta = h.negbeta;
+  a.kltc = g.kltc;
+  a.out = h.out;
+  a.out_gs = h.out_gs;
+  a.out_rs = h.out_rs;
+  a.out_ts = h.out_ts;
+  a.hdr = h.hdr;
+  a.mark_pos = h.mark_pos;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, h.wt16, uint64_t(g.d), uint64_t(g.n_w) * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_strided(&mx, h.x, uint64_t(g.d), uint64_t(h.rows) * h.groups, uint64_t(h.x_rs) * 2, 64,
+                        uint32_t(a.nr), CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const size_t smem = RowsLayout<D>::bytes(a.nr) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_hash_rows_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid((h.rows + a.nr - 1) / a.nr, g.nt, h.groups);
+  k_hash_rows_tc<D><<<grid, kRowsWarps * 32, smem, st>>>(mw, mx, a, g.L, g.K, g.tpt);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st) {
+  if (h.rows <= 0 || h.groups <= 0 || g.nt == 0) return cudaSuccess;
+  return g.d == 128 ? launch_rows_tc<128>(g, h, st) : launch_rows_tc<64>(g, h, st);
+}
 
 cudaError_t launch_hash_keys_tc(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,
                                 cudaStream_t st, bool* used) {

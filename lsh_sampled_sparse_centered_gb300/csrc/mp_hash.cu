@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(256) k_center_parts(const T* __restrict__ keys
 
 __global__ void k_center_final(const float* __restrict__ cparts, float* __restrict__ center,
                                __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ ones,
+                               float* __restrict__ negbeta,
                                const __nv_bfloat16* __restrict__ wt16, int d,
                                int kltc, int parts, int count, int units_per_w, int64_t w_stride,
                                DevHeader* hdr, int n_prefill) {
@@ -127,6 +128,7 @@ __global__ void k_center_final(const float* __restrict__ cparts, float* __restri
       float sacc = 0.f;
       for (int dim = 0; dim < d; ++dim) sacc = fmaf(__bfloat162float(row[dim]), c[dim], sacc);
       const float nb = -sacc;
+      negbeta[int64_t(u) * kltc + j] = nb;
       const __nv_bfloat16 hi = __float2bfloat16_rn(nb);
       const float r1 = nb - __bfloat162float(hi);
       const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
@@ -164,7 +166,7 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
-  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.wt16, g.d,
+  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.negbeta, t.wt16, g.d,
                                                           g.kltc, g.parts, hi - lo, g.batch * g.kvh,
                                                           w_stride, t.hdr, n_prefill);
   return cudaGetLastError();
@@ -180,19 +182,14 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
 // ---------------------------------------------------------------------------------
 constexpr int kHashCols = 256;
 
-__device__ __forceinline__ void w4(const float* p, float (&w)[4]) {
-  w[0] = p[0];
-  w[1] = p[1];
-  w[2] = p[2];
-  w[3] = p[3];
+// four consecutive W elements of a shared-memory row as two packed fp32 pairs
+__device__ __forceinline__ void w4(const float* p, uint64_t& a, uint64_t& b) {
+  a = pk2(p[0], p[1]);
+  b = pk2(p[2], p[3]);
 }
-__device__ __forceinline__ void w4(const __nv_bfloat16* p, float (&w)[4]) {
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + 2));
-  w[0] = a.x;
-  w[1] = a.y;
-  w[2] = b.x;
-  w[3] = b.y;
+__device__ __forceinline__ void w4(const __nv_bfloat16* p, uint64_t& a, uint64_t& b) {
+  a = bf2_to_f2(*reinterpret_cast<const uint32_t*>(p));
+  b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(p + 2));
 }
 
 template <typename T, typename WT, int R>
@@ -249,24 +246,23 @@ __global__ void __launch_bounds__(kHashCols) k_hash_rows(HashRowsArgs a, int d, 
   }
   __syncthreads();
   const WT* wrow = reinterpret_cast<const WT*>(wsm + tid * wstride);
-  float acc[R];
+  // even and odd dimensions accumulate in the two halves of a packed pair
+  uint64_t acc[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int r = 0; r < R; ++r) acc[r] = 0ull;
   for (int d0 = 0; d0 < d; d0 += 4) {
-    float w[4];
-    w4(wrow + d0, w);
+    uint64_t wa, wb;
+    w4(wrow + d0, wa, wb);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const float4 x = *reinterpret_cast<const float4*>(xs + r * d + d0);
-      acc[r] = fmaf(w[0], x.x, acc[r]);
-      acc[r] = fmaf(w[1], x.y, acc[r]);
-      acc[r] = fmaf(w[2], x.z, acc[r]);
-      acc[r] = fmaf(w[3], x.w, acc[r]);
+      acc[r] = fma2(wa, pk2(x.x, x.y), acc[r]);
+      acc[r] = fma2(wb, pk2(x.z, x.w), acc[r]);
     }
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const uint32_t m = __ballot_sync(0xffffffffu, acc[r] > 0.f);
+    const uint32_t m = __ballot_sync(0xffffffffu, lo2(acc[r]) + hi2(acc[r]) > 0.f);
     if (lane == 0) bits[r][warp] = m;
   }
   if (tid < R) bits[tid][kHashCols / 32] = 0u;

@@ -51,6 +51,7 @@ struct TablesPtrs {
   float* center;
   __nv_bfloat16* beta;   // [U][kltc][16]: -W^T c as three bf16 terms per column
   __nv_bfloat16* ones;   // [128][16]: (1, 1, 1, 0, ...) per row
+  float* negbeta;        // [U][kltc]: -W^T c
   float* wt32;
   __nv_bfloat16* wt16;
   float* cparts;
@@ -89,7 +90,25 @@ struct HashRowsArgs {
   int mark_pos;
 };
 
+// Rows hashed on the tensor cores (bf16 rows and W, d = 64 or 128): `groups` groups of
+// `rows` rows, row r of group g at x + (g * rows + r) * x_rs elements; group g uses W
+// matrix g / groups_per_w (when W is per layer). negbeta != nullptr: the rows are keys
+// of units g * rows + r, centered by adding -beta in the epilogue, and the launch also
+// raises the appended end to mark_pos + 1.
+struct RowsHashTc {
+  const __nv_bfloat16* x;
+  int64_t x_rs;
+  int rows, groups, groups_per_w;
+  const __nv_bfloat16* wt16;
+  const float* negbeta;  // [U][kltc]
+  uint16_t* out;
+  int64_t out_gs, out_rs, out_ts;
+  DevHeader* hdr;
+  int mark_pos;
+};
+
 // ---- launchers (each returns cudaError_t of the launch) ----
+cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st);
 cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st);
 cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,
                           cudaStream_t st);
@@ -121,6 +140,44 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Packed fp32 pairs (PTX .f32x2 arithmetic, sm_100 and later): one instruction works on
+// two lanes of a 64-bit register, each half rounded exactly like the scalar
+// instruction, so a pair op equals two scalar fmaf / __fadd_rn / __fmul_rn calls.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float hi2(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// two bf16 (low element first) as a packed fp32 pair: widening is exact
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
 #endif
 
 }  // namespace mp

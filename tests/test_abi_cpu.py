@@ -65,7 +65,7 @@ def test_config_validation(mp):
 def test_layouts_are_aligned_disjoint_and_sized(mp):
     c = _cfg(mp, layers=2, w_per_layer=True)
     t = mp.mp_tables_layout_get(c)
-    names = ["header", "center", "beta", "ones", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets",
+    names = ["header", "center", "beta", "ones", "negbeta_f32", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets",
              "csr_ids"]
     offs = [getattr(t, n) for n in names]
     assert all(o % 256 == 0 for o in offs)
