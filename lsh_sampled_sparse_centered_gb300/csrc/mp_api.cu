@@ -117,7 +117,7 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
     o->csr_offsets = off;
     off = align256(off + U * L * uint64_t(g.nseg) * (uint64_t(g.nb) + 1) * 2);
     o->csr_ids = off;
-    off = align256(off + U * L * cap * 2);
+    off = align256(off + U * L * cap * 2 + 16);  // +16: aligned 16-byte chunk reads past the last id
   } else {
     o->planes = off;
     off = align256(off + U * L * uint64_t(g.K) * g.cw * 4);

@@ -22,8 +22,7 @@ namespace mp {
 // ascending token order, then the exact tokens (bit 31 set).
 constexpr int kMatchWarps = 8;
 
-template <int PER>
-__global__ void __launch_bounds__(kMatchWarps * 32, 4) k_match_csr(DevHeader* hdr,
+__global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
                                                    const uint16_t* __restrict__ off,
@@ -63,93 +62,69 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 4) k_match_csr(DevHeader* hd
 
   if (built && hi > lo) {
     // tokens hashed at build time: the query's bucket in every (table, segment). The
-    // bucket ranges are fetched first (one round trip for all of them); then each warp
-    // takes TB buckets at a time (buckets average 32768 / 2^K entries) and marks them.
+    // bucket ranges are fetched first (one round trip for all of them, read as 8-byte
+    // chunks of 4 offsets), then the buckets' ids.
     const int64_t tbase = int64_t(unit) * L;
     const int lo_b = min(s, n0);  // first token bucketed at build time
     const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
     const int pairs = L * nsu;
+    auto elem = [](uint2 w, uint32_t q) -> uint32_t { return ((q & 2u) ? w.y : w.x) >> ((q & 1u) * 16u) & 0xffffu; };
     for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
       const int t = p / nsu, sg = p - (p / nsu) * nsu;
-      const uint16_t* o = off + ((tbase + t) * nseg + sg) * (nb + 1);
-      const int code = qc[t];
-      const uint32_t b0 = __ldg(&o[code]), b1 = __ldg(&o[code + 1]);
+      const uint16_t* o = off + ((tbase + t) * nseg + sg) * (nb + 1) + qc[t];
+      const uintptr_t oa = reinterpret_cast<uintptr_t>(o);
+      const uint32_t pos = uint32_t(oa & 7u) >> 1;
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(oa & ~uintptr_t(7)));
+      const uint32_t b0 = elem(w, pos);
+      const uint32_t b1 = pos < 3u ? elem(w, pos + 1u) : uint32_t(__ldg(o + 1));
       // {position of the bucket in the unit's id arrays, size | segment << 16}
       bkt[p] = make_uint2(uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0, (b1 - b0) | (uint32_t(sg) << 16));
     }
     __syncthreads();
     const uint16_t* idu = ids + tbase * cap;
-    auto mark = [&](uint32_t tok) {
-      if (tok < uint32_t(hi)) {
-        if (bytes) {
-          atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
-        } else {
-          const uint32_t bit = 1u << (tok & 31);
-          const uint32_t old = atomicOr(&seen1[tok >> 5], bit);
-          if (old & bit) atomicOr(&seen2[tok >> 5], bit);
-        }
-      }
-    };
-    // lane i loads entries i, i + 32, ... (PER of them) of each of TB buckets: 32 loads
-    // in flight per lane. All first marks of a batch are issued before the second ones,
-    // so that the atomics do not wait on one another. The rare bucket above 32 * PER
-    // entries finishes in a second loop, 4 loads per lane at a time.
-    constexpr int TB = 32 / PER;
-    for (int p0 = warp * TB; p0 < pairs; p0 += kMatchWarps * TB) {
-      uint32_t tk[TB][PER];
-      bool big = false;
+    // Each thread walks whole buckets (bucket p = thread, thread + 256, ...): the ids are
+    // read as 16-byte aligned chunks of 8, two chunks in flight, and every id is marked
+    // by the thread itself, so all lanes do useful work whatever the bucket sizes. Within
+    // a group of two chunks the first marks are all issued before the second ones, so
+    // that the atomics do not wait on one another.
+    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
+      const uint2 e = bkt[p];
+      const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(idu + e.x);
+      const uint32_t skip = uint32_t(a0 & 15u) >> 1;  // ids of the first chunk before the bucket
+      const uint4* ch = reinterpret_cast<const uint4*>(a0 & ~uintptr_t(15));
+      const uint32_t nch = (skip + sz + 7u) >> 3;
+      for (uint32_t c0 = 0; c0 < nch; c0 += 2) {
+        uint4 v[2];
 #pragma unroll
-      for (int j = 0; j < TB; ++j) {
-        const bool live = p0 + j < pairs;
-        const uint2 e = live ? bkt[p0 + j] : make_uint2(0u, 0u);
-        const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
-        big |= sz > 32u * PER;
+        for (int k = 0; k < 2; ++k) v[k] = c0 + k < nch ? __ldg(ch + c0 + k) : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t dup = 0;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const uint32_t i = 32u * k + lane;
-          tk[j][k] = i < sz ? tok0 + __ldg(&idu[e.x + i]) : 0xffffffffu;
-        }
-      }
-      if (bytes) {
+        for (int k = 0; k < 2; ++k)
 #pragma unroll
-        for (int j = 0; j < TB; ++j)
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            const uint32_t tok = tk[j][k];
-            if (tok < uint32_t(hi)) atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
-          }
-      } else {
-        uint64_t dup = 0;
-#pragma unroll
-        for (int j = 0; j < TB; ++j)
-#pragma unroll
-          for (int k = 0; k < PER; ++k) {
-            const uint32_t tok = tk[j][k];
-            if (tok < uint32_t(hi)) {
-              const uint32_t bit = 1u << (tok & 31);
-              if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1ull << (j * PER + k);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t word = (q < 2) ? v[k].x : (q < 4) ? v[k].y : (q < 6) ? v[k].z : v[k].w;
+            const uint32_t i = (c0 + k) * 8u + uint32_t(q) - skip;  // index in the bucket (wraps if < 0)
+            const uint32_t tok = tok0 + ((word >> (16 * (q & 1))) & 0xffffu);
+            if (i < sz && tok < uint32_t(hi)) {
+              if (bytes) {
+                atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
+              } else {
+                const uint32_t bit = 1u << (tok & 31);
+                if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1u << (k * 8 + q);
+              }
             }
           }
+        if (dup) {
 #pragma unroll
-        for (int j = 0; j < TB; ++j)
+          for (int k = 0; k < 2; ++k)
 #pragma unroll
-          for (int k = 0; k < PER; ++k)
-            if ((dup >> (j * PER + k)) & 1ull) atomicOr(&seen2[tk[j][k] >> 5], 1u << (tk[j][k] & 31));
-      }
-      if (__any_sync(0xffffffffu, big)) {
-        for (int j = 0; j < TB && p0 + j < pairs; ++j) {
-          const uint2 e = bkt[p0 + j];
-          const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
-          for (uint32_t i0 = 32u * PER; i0 < sz; i0 += 128u) {
-            uint32_t t4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t i = i0 + 32u * k + lane;
-              t4[k] = i < sz ? tok0 + __ldg(&idu[e.x + i]) : 0xffffffffu;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mark(t4[k]);
-          }
+            for (int q = 0; q < 8; ++q)
+              if ((dup >> (k * 8 + q)) & 1u) {
+                const uint32_t word = (q < 2) ? v[k].x : (q < 4) ? v[k].y : (q < 6) ? v[k].z : v[k].w;
+                const uint32_t tok = tok0 + ((word >> (16 * (q & 1))) & 0xffffu);
+                atomicOr(&seen2[tok >> 5], 1u << (tok & 31));
+              }
         }
       }
     }
@@ -199,17 +174,10 @@ cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, cons
   const int nwords = (hi + 31) >> 5;
   const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
   const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 8 + size_t(g.L) * 2 + 16;
-  // entries per lane and bucket from the mean bucket size of a segment
-  const int mean = std::min(kCsrSeg, n) >> g.K;
-  auto go = [&](auto kern) {
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    kern<<<g.queries, kMatchWarps * 32, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists, dp.list_len,
-                                                    dp.sample_count, dp.counters, n, g.s, g.w, g.L, g.nb, g.cap,
-                                                    g.nseg, g.group, g.threshold);
-  };
-  if (mean <= 24) go(k_match_csr<1>);
-  else if (mean <= 48) go(k_match_csr<2>);
-  else go(k_match_csr<4>);
+  cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  k_match_csr<<<g.queries, kMatchWarps * 32, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists,
+                                                         dp.list_len, dp.sample_count, dp.counters, n, g.s, g.w, g.L,
+                                                         g.nb, g.cap, g.nseg, g.group, g.threshold);
   return cudaGetLastError();
 }
 
