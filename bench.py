@@ -34,7 +34,7 @@ DEFAULT_WORKLOAD = 2
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
@@ -92,7 +92,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -108,7 +108,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -360,6 +360,32 @@ def run_ours(args, rank, world, local):
     return line, job
 
 
+# kernel -> source file whose contents the recorded DRAM counters belong to
+KERNEL_SOURCE = {
+    "attend": "mp_decode.cu", "match_csr": "mp_decode.cu", "hash_keys_tc": "mp_gemm.cu",
+    "hash_query": "mp_gemm.cu", "hash_append": "mp_gemm.cu", "csr_build": "mp_csr.cu", "center": "mp_hash.cu",
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def measured_traffic(kernel: str, algorithmic_per_launch: float):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu counters:
+    the captured launch's traffic per algorithmic byte (or flop), times this launch's
+    algorithmic amount. None when no counters are recorded or the kernel's source file
+    has changed since they were taken."""
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["kernels"][kernel]
+        src = os.path.join(ROOT, "lsh_sampled_sparse_centered_gb300", "csrc", KERNEL_SOURCE[kernel])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return float(rec["dram_bytes_per_algorithmic_unit"]) * algorithmic_per_launch
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
     """Per-kernel average durations and algorithmic work for one job; roofline of the
     kernel with the largest share of device time."""
@@ -403,7 +429,8 @@ def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
     kind = work[dom][0]
     roof = {"kernel": dom, "bound": "hbm" if kind == "bytes" else "tensor", "achieved": kd["achieved"],
             "peak": hbm if kind == "bytes" else tc, "unit": kd["unit"], "frac": kd["frac"],
-            "traffic": None, "peak_source": pk["source"] + (" (sustained)" if kind != "bytes" else "")}
+            "traffic": measured_traffic(dom, kd["algorithmic_per_launch"]),
+            "peak_source": pk["source"] + (" (sustained)" if kind != "bytes" else "")}
     # whole-job roofline: bytes at HBM bandwidth + hashing flops at tensor peak
     t_roof = sum(v[1] / (hbm * 1e9) for k, v in work.items() if v[0] == "bytes" and k in prof)
     t_roof += sum(v[1] / (tc * 1e12) for k, v in work.items() if v[0] == "flops" and k in prof)
