@@ -114,9 +114,9 @@ typedef struct mp_tables_layout {
   uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: the same in bf16 (bf16 configs only, else 0) */
   uint64_t center_parts; /* float [U][parts][d]: partial sums while building */
   uint64_t codes;        /* uint16 [U][L][capacity]: code of every hashed token, table-major */
-  uint64_t csr_offsets;  /* uint16 [U][L][NS][NB+1]: per table and 32768-token segment of [n_sink, n_prefill),
-                            the start of each bucket within the segment (CSR mode, else 0);
-                            NS = ceil(capacity / 32768) */
+  uint64_t csr_offsets;  /* uint16 [U][L][NB+1][NS]: per table, bucket b and 32768-token segment s of
+                            [n_sink, n_prefill), the start of bucket b within segment s (element
+                            [NB][s]: the segment's length) (CSR mode, else 0); NS = ceil(capacity / 32768) */
   uint64_t csr_ids;      /* uint16 [U][L][capacity]: element 32768*s + i is the i-th id of segment s in
                             bucket order, as an offset from the segment's first token; the order inside
                             a bucket is unspecified (CSR mode, else 0) */
@@ -138,7 +138,8 @@ typedef struct mp_decode_layout {
   uint64_t lists;        /* uint32 [Q][capacity]: token ids, S ascending then exact tokens
                             (bit 31 set on exact tokens) */
   uint64_t partials;     /* float [Q][splits_max][d+2]: split-K partial (m, l, acc[d]) */
-  uint64_t counters;     /* uint32 [Q]: split-K completion counters */
+  uint64_t counters;     /* uint32 [Q + 1]: split-K completion counters, then the attention's
+                            work-queue head */
   uint64_t sample_bits;  /* uint32 [Q][CW]: sampled-token bitmaps (scan mode, else 0) */
   int32_t splits_max;
   int32_t reserved;

@@ -145,7 +145,7 @@ static void decode_layout(const Geometry& g, mp_decode_layout* o) {
   o->partials = off;
   off = align256(off + Q * kSplitsMax * uint64_t(g.d + 2) * 4);
   o->counters = off;
-  off = align256(off + Q * 4);
+  off = align256(off + (Q + 1) * 4);
   if (g.match == MP_MATCH_SCAN) {
     o->sample_bits = off;
     off = align256(off + Q * uint64_t(g.cw) * 4);
@@ -235,7 +235,7 @@ static int choose_splits(const Geometry& g, int n) {
   const int lo = std::min(g.s, n);
   const int hi = std::max(lo, n - g.w);
   const double est = double(n - (hi - lo)) + frac * double(hi - lo);
-  int s = int(std::ceil(est / 256.0));
+  int s = int(std::ceil(est / 1024.0));
   if (s < 1) s = 1;
   if (s > kSplitsMax) s = kSplitsMax;
   return s;

@@ -61,15 +61,17 @@ __global__ void __launch_bounds__(kCsrThreads, 2) k_csr_build(const uint16_t* __
     wsum[lane] = v;
   }
   __syncthreads();
-  uint16_t* o = off + (table * nseg + s) * int64_t(nb + 1);
+  // offsets of the table, bucket-major with the segments innermost: the starts of one
+  // bucket in all segments (and those of the next bucket) share a cache line
+  uint16_t* o = off + table * int64_t(nb + 1) * nseg + s;
   uint32_t base = x - local + (warp > 0 ? wsum[warp - 1] : 0u);
   for (int b = b0; b < b1; ++b) {
     const uint32_t cnt = cursor[b];
     cursor[b] = base;
-    o[b] = uint16_t(base);
+    o[int64_t(b) * nseg] = uint16_t(base);
     base += cnt;
   }
-  if (tid == 0) o[nb] = uint16_t(m);
+  if (tid == 0) o[int64_t(nb) * nseg] = uint16_t(m);
   __syncthreads();
 
   // pass 2: placement

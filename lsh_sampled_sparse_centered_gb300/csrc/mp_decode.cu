@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
   const int app_end = hdr->appended_end;
   if (threadIdx.x == 0) {
     counters[qh] = 0u;
+    if (qh == 0) counters[gridDim.x] = 0u;  // the attention's work queue
     if (!built) atomicOr(&hdr->status, MP_STATUS_NOT_BUILT);
     else if (hi > app_end) atomicOr(&hdr->status, MP_STATUS_APPEND_GAP);
   }
@@ -62,23 +63,20 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
 
   if (built && hi > lo) {
     // tokens hashed at build time: the query's bucket in every (table, segment). The
-    // bucket ranges are fetched first (one round trip for all of them, read as 8-byte
-    // chunks of 4 offsets), then the buckets' ids.
+    // bucket ranges are fetched first, one table per thread (the starts of a bucket in
+    // all segments and those of the next bucket share a cache line), then the ids.
     const int64_t tbase = int64_t(unit) * L;
     const int lo_b = min(s, n0);  // first token bucketed at build time
     const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
     const int pairs = L * nsu;
-    auto elem = [](uint2 w, uint32_t q) -> uint32_t { return ((q & 2u) ? w.y : w.x) >> ((q & 1u) * 16u) & 0xffffu; };
-    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-      const int t = p / nsu, sg = p - (p / nsu) * nsu;
-      const uint16_t* o = off + ((tbase + t) * nseg + sg) * (nb + 1) + qc[t];
-      const uintptr_t oa = reinterpret_cast<uintptr_t>(o);
-      const uint32_t pos = uint32_t(oa & 7u) >> 1;
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(oa & ~uintptr_t(7)));
-      const uint32_t b0 = elem(w, pos);
-      const uint32_t b1 = pos < 3u ? elem(w, pos + 1u) : uint32_t(__ldg(o + 1));
-      // {position of the bucket in the unit's id arrays, size | segment << 16}
-      bkt[p] = make_uint2(uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0, (b1 - b0) | (uint32_t(sg) << 16));
+    for (int t = threadIdx.x; t < L; t += blockDim.x) {
+      const uint16_t* o = off + (tbase + t) * int64_t(nb + 1) * nseg + int64_t(qc[t]) * nseg;
+      for (int sg = 0; sg < nsu; ++sg) {
+        const uint32_t b0 = __ldg(o + sg), b1 = __ldg(o + nseg + sg);
+        // {position of the bucket in the unit's id arrays, size | segment << 16}
+        bkt[t * nsu + sg] =
+            make_uint2(uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0, (b1 - b0) | (uint32_t(sg) << 16));
+      }
     }
     __syncthreads();
     const uint16_t* idu = ids + tbase * cap;
@@ -302,8 +300,15 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
   __shared__ float sm_acc[NW][D];
   __shared__ int sm_last;
   __shared__ uint32_t sl[kListChunk];
-  // persistent: the CTA walks items (query head, slice) = (item / P, item % P)
-  for (int item = blockIdx.x; item < queries * P; item += gridDim.x) {
+  // persistent: the CTAs take items (query head, slice) = (item / P, item % P) from a
+  // work queue (counters[queries], zeroed by the match kernel), so that a CTA that
+  // drew short slices takes more of them
+  __shared__ int s_item;
+  for (;;) {
+  if (threadIdx.x == 0) s_item = int(atomicAdd(&counters[queries], 1u));
+  __syncthreads();
+  const int item = s_item;
+  if (item >= queries * P) break;
   const int qh = item / P, split = item - (item / P) * P;
   const int unit = qh / group;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(256) k_compact(DevHeader* hdr, const uint32_t*
   const bool built = hdr->magic == kMagic;
   if (threadIdx.x == 0) {
     counters[qh] = 0u;
+    if (qh == 0) counters[gridDim.x] = 0u;  // the attention's work queue
     if (!built) atomicOr(&hdr->status, MP_STATUS_NOT_BUILT);
     else if (hi > hdr->appended_end) atomicOr(&hdr->status, MP_STATUS_APPEND_GAP);
   }

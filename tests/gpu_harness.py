@@ -80,7 +80,7 @@ class GpuRun:
         i0 = self.tl.csr_ids + u * wl.L * wl.capacity * 2
         off = self.tables[o0: o0 + tables * ns * (nb + 1) * 2].view(torch.int16)
         ids = self.tables[i0: i0 + tables * wl.capacity * 2].view(torch.int16)
-        return ((off.cpu().numpy().astype(np.int64) & 0xFFFF).reshape(tables, ns, nb + 1),
+        return ((off.cpu().numpy().astype(np.int64) & 0xFFFF).reshape(tables, nb + 1, ns).transpose(0, 2, 1),
                 (ids.cpu().numpy().astype(np.int64) & 0xFFFF).reshape(tables, wl.capacity))
 
     def unit_planes(self, u: int, tables: int) -> np.ndarray:
@@ -95,15 +95,6 @@ class GpuRun:
         U = wl.layers * wl.batch * wl.kv_heads
         return self._view(self.tables, self.tl.center, U * wl.head_dim, torch.float32).cpu().numpy().reshape(
             U, wl.head_dim)
-
-    def csr(self):
-        wl = self.wl
-        U = wl.layers * wl.batch * wl.kv_heads
-        nb = self.tl.n_buckets
-        off = self._view(self.tables, self.tl.csr_offsets, U * wl.L * (nb + 1), torch.int32)
-        ids = self._view(self.tables, self.tl.csr_ids, U * wl.L * wl.capacity, torch.int32)
-        return (off.cpu().numpy().astype(np.int64).reshape(U, wl.L, nb + 1),
-                ids.cpu().numpy().astype(np.int64).reshape(U, wl.L, wl.capacity))
 
     def decode_state(self):
         wl = self.wl
