@@ -14,7 +14,7 @@
 // key tiles (A, 128 x d) and W column tiles (B, 256 x d) with TMA into 128B-swizzled
 // shared memory; warp 1 issues tcgen05.mma (M=128, N=256, K=16 steps) into one of two
 // 256-column fp32 accumulators in tensor memory; warps 2..13 (three per tensor-memory
-// lane quarter, each owning a third of the tile's tables) read the accumulator with
+// lane quarter, each owning a part of the tile's tables) read the accumulator with
 // tcgen05.ld, form the codes and store them. W columns are laid out so that every
 // 256-column tile holds floor(256/K) whole tables: no code straddles two tiles.
 // All waits are bounded: on expiry the kernel records MP_STATUS_WAIT_TIMEOUT and stops.
@@ -29,7 +29,8 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
-constexpr int kEpiWarps = 12;  // three per TMEM lane quarter
+constexpr int kEpiWarps = 12;  // kParts per TMEM lane quarter
+constexpr int kParts = kEpiWarps / 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
@@ -144,14 +145,14 @@ __device__ __forceinline__ uint32_t sign_word(const uint32_t (&r)[32]) {
   return ~__brev((w0 << 24) | (w1 << 16) | (w2 << 8) | w3);
 }
 
-// Codes of one third of a 256-column tile with K known at compile time: the column,
+// Codes of one part of a 256-column tile with K known at compile time: the column,
 // word and shift of every code are constants, so cutting a code is one or two shifts.
-template <int KC, int THIRD>
+template <int KC, int PART>
 __device__ __forceinline__ void epi_tile_k(uint32_t tbase, uint16_t* codes, int64_t u, int L, int cap, int row,
                                            bool store, int n) {
   constexpr int TPT = 256 / KC;
-  constexpr int TP = (TPT + 2) / 3;
-  constexpr int TL0 = (THIRD * TP < TPT) ? THIRD * TP : TPT;
+  constexpr int TP = (TPT + kParts - 1) / kParts;
+  constexpr int TL0 = (PART * TP < TPT) ? PART * TP : TPT;
   constexpr int TL1 = (TL0 + TP < TPT) ? TL0 + TP : TPT;
   if constexpr (TL0 < TL1) {
     constexpr int C0 = TL0 * KC, C1 = TL1 * KC;
@@ -304,9 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue: 12 warps, 3 per TMEM lane quarter ----------------
     const int e = warp - 2;
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31 are reachable by this warp
-    const int third = e >> 2;          // which third of the tile's tables
-    const int t_per = (tpt + 2) / 3;
-    const int tl0 = min(tpt, third * t_per), tl1 = min(tpt, tl0 + t_per);
+    const int part = e >> 2;           // which part of the tile's tables
+    const int t_per = (tpt + kParts - 1) / kParts;
+    const int tl0 = min(tpt, part * t_per), tl1 = min(tpt, tl0 + t_per);
     const uint32_t mask = (1u << K) - 1u;
     uint32_t ac = 0;
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
@@ -327,9 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tlast = min(n * tpt + tl1, L);  // exclusive
         if constexpr (KT > 0) {
           const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(cs * kTileN);
-          if (third == 0) epi_tile_k<KT, 0>(tbase, codes, u, L, cap, row, store, n);
-          else if (third == 1) epi_tile_k<KT, 1>(tbase, codes, u, L, cap, row, store, n);
-          else epi_tile_k<KT, 2>(tbase, codes, u, L, cap, row, store, n);
+          if (part == 0) epi_tile_k<KT, 0>(tbase, codes, u, L, cap, row, store, n);
+          else if (kParts > 1 && part == 1) epi_tile_k<KT, (kParts > 1 ? 1 : 0)>(tbase, codes, u, L, cap, row, store, n);
+          else if (kParts > 2 && part == 2) epi_tile_k<KT, (kParts > 2 ? 2 : 0)>(tbase, codes, u, L, cap, row, store, n);
+          else if (kParts > 3) epi_tile_k<KT, (kParts > 3 ? 3 : 0)>(tbase, codes, u, L, cap, row, store, n);
         } else if (tfirst < tlast) {
           const int c0 = tl0 * K, c1 = (tlast - n * tpt) * K;  // column range within the tile
           const uint32_t tbase = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(cs * kTileN);
