@@ -40,6 +40,9 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="sampled budget and step time over the pages' (K, L) grid, centering on and off "
+                         "(one layer of the workload; one JSON line per grid point)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every call from Python instead of replaying the captured job graph")
     return ap.parse_args()
@@ -243,13 +246,13 @@ def decode_state_stats(job, torch):
               & 0xFFFF).view(Q, wl.L)
         nb, nseg = tl.n_buckets, -(-wl.capacity // 32768)
         off = (job.tables[tl.csr_offsets: tl.csr_offsets + 2 * U * wl.L * nseg * (nb + 1)].view(torch.int16)
-               .to(torch.int64) & 0xFFFF).view(U, wl.L, nseg, nb + 1)
+               .to(torch.int64) & 0xFFFF).view(U, wl.L, nb + 1, nseg)  # bucket-major, segments innermost
         unit = torch.arange(Q, device=qc.device) // wl.group
         t = torch.arange(wl.L, device=qc.device)
         used = -(-(wl.n_prefill - min(wl.n_sink, wl.n_prefill)) // 32768)
         for sg in range(used):
-            b0 = off[unit[:, None], t[None, :], sg, qc]
-            b1 = off[unit[:, None], t[None, :], sg, qc + 1]
+            b0 = off[unit[:, None], t[None, :], qc, sg]
+            b1 = off[unit[:, None], t[None, :], qc + 1, sg]
             walked = walked + (b1 - b0).sum()
     return torch.stack([ln.sum(), ns.sum(), walked])
 
@@ -576,8 +579,64 @@ def run_reference(args, rank, world):
     }
 
 
+SWEEP_GRID = [(8, 75), (8, 90), (9, 120), (10, 150), (10, 220), (10, 300), (11, 300)]
+
+
+def run_sweep(args):
+    """(K, L) grid of the pages with centering on and off on one layer of the workload:
+    measured sampled fraction (the GPU's |S| / |R|), the isotropic closed form, the
+    list entries per query head and the device time per decode step."""
+    import torch
+
+    import workloads as WL
+    import __graft_entry__
+    __graft_entry__.build()
+    import lsh_sampled_sparse_centered_gb300 as mp
+
+    dev = torch.device("cuda", 0)
+    base = WL.WORKLOADS[args.workload].replace(layers=1, steps=8)
+    stream = torch.cuda.Stream(device=dev)
+    for K, L in SWEEP_GRID:
+        for centering in (True, False):
+            wl = base.replace(K=K, L=L, name=f"{base.name}-1L-K{K}-L{L}")
+            with torch.cuda.stream(stream):
+                job = Job(mp, wl, dev, stream)
+                job.cfg.no_centering = 0 if centering else 1
+            stats = torch.zeros(3, dtype=torch.int64, device=dev)
+            job.hook = lambda s, n: stats.add_(decode_state_stats(job, torch))
+            with torch.cuda.stream(stream):
+                job.run()  # warm-up, and the sampled-set statistics
+            torch.cuda.synchronize()
+            assert mp.mp_get_status(job.tables, stream=job.sp) == 0
+            job.hook = None
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            with torch.cuda.stream(stream):
+                ev[0].record(stream)
+                job.build()
+                ev[1].record(stream)
+                job.decode_steps()
+                ev[2].record(stream)
+            torch.cuda.synchronize()
+            entries, sampled, _ = [int(v) for v in stats.cpu()]
+            Q = wl.layers * wl.batch * wl.q_heads
+            region = sum(max(0, wl.seq_len(t) - wl.window - min(wl.n_sink, wl.seq_len(t))) for t in range(wl.steps)) * Q
+            x = 0.5 ** K
+            print(json.dumps({
+                "sweep": "budget", "workload": wl.name, "K": K, "L": L, "centering": centering,
+                "sampled_fraction": sampled / region, "closed_form_fraction_isotropic":
+                    1 - (1 - x) ** L - L * x * (1 - x) ** (L - 1),
+                "list_entries_per_query": entries / (Q * wl.steps),
+                "build_ms": ev[0].elapsed_time(ev[1]),
+                "us_per_decode_step": 1e3 * ev[1].elapsed_time(ev[2]) / wl.steps}), flush=True)
+            del job
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -92,7 +92,10 @@ typedef struct mp_config {
   int32_t match_mode;  /* MP_MATCH_AUTO, MP_MATCH_CSR or MP_MATCH_SCAN */
   int32_t threshold;   /* minimum colliding tables for a key to be sampled, 1..7 (pages: 2);
                           above 2 it needs L <= 255 and, in CSR mode, capacity <= 196608 */
-  int32_t reserved[4]; /* must be zero */
+  int32_t no_centering; /* 0 (default): keys are centered by their prefill mean before hashing
+                           (pages §4.3 "Data pre-processing"); 1: hashed uncentered, c = 0 (the
+                           pages' centering ablation) */
+  int32_t reserved[3]; /* must be zero */
 } mp_config;
 
 /* Byte offsets (from the start of the tables buffer) of the arrays the library keeps

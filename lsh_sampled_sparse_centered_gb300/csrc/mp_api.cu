@@ -34,8 +34,9 @@ static int check_config(const mp_config* c) {
   if (c->match_mode != MP_MATCH_AUTO && c->match_mode != MP_MATCH_CSR && c->match_mode != MP_MATCH_SCAN)
     return MP_ERR_INVALID_ARG;
   if (c->threshold < 1 || c->threshold > c->L) return MP_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
+  if (c->no_centering != 0 && c->no_centering != 1) return MP_ERR_INVALID_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return MP_ERR_UNSUPPORTED;
   if (c->K > kMaxK || c->L > kMaxL || c->capacity > kMaxCapacity) return MP_ERR_UNSUPPORTED;
   // thresholds above 2: at most 7 (3-bit counters in the scan), L <= 255 (byte counters
@@ -73,6 +74,7 @@ static Geometry geometry(const mp_config* c) {
   g.dtype = c->dtype;
   g.w_per_layer = c->w_per_layer;
   g.threshold = c->threshold;
+  g.no_center = c->no_centering;
   g.group = c->q_heads / c->kv_heads;
   g.units = c->layers * c->batch * c->kv_heads;
   g.queries = c->layers * c->batch * c->q_heads;

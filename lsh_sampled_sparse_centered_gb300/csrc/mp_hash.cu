@@ -107,13 +107,13 @@ __global__ void k_center_final(const float* __restrict__ cparts, float* __restri
                                float* __restrict__ negbeta,
                                const __nv_bfloat16* __restrict__ wt16, int d,
                                int kltc, int parts, int count, int units_per_w, int64_t w_stride,
-                               DevHeader* hdr, int n_prefill) {
+                               DevHeader* hdr, int n_prefill, int no_center) {
   extern __shared__ float c[];  // [d]
   const int u = blockIdx.x;
   for (int dim = threadIdx.x; dim < d; dim += blockDim.x) {
     float s = 0.f;
     for (int p = 0; p < parts; ++p) s += cparts[(int64_t(u) * parts + p) * d + dim];
-    const float v = count > 0 ? s / float(count) : 0.f;
+    const float v = (count > 0 && !no_center) ? s / float(count) : 0.f;
     c[dim] = v;
     center[int64_t(u) * d + dim] = v;
   }
@@ -168,7 +168,7 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
   const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.negbeta, t.wt16, g.d,
                                                           g.kltc, g.parts, hi - lo, g.batch * g.kvh,
-                                                          w_stride, t.hdr, n_prefill);
+                                                          w_stride, t.hdr, n_prefill, g.no_center);
   return cudaGetLastError();
 }
 

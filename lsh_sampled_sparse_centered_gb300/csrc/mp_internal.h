@@ -31,6 +31,7 @@ static_assert(sizeof(DevHeader) == 256, "header size");
 // Sizes derived from an mp_config.
 struct Geometry {
   int layers, batch, kvh, qh, d, K, L, s, w, cap, dtype, w_per_layer, threshold;
+  int no_center;  // 1: keys hashed uncentered (c = 0)
   int group;    // q_heads / kv_heads
   int units;    // layers * batch * kv_heads
   int queries;  // layers * batch * q_heads

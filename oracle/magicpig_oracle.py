@@ -265,12 +265,14 @@ class HeadTables:
     """
 
     def __init__(self, keys, W, K: int, L: int, n_sink: int, n_prefill: int,
-                 n_total: int | None = None):
+                 n_total: int | None = None, centering: bool = True):
         keys = _f64(keys)
         n_total = keys.shape[0] if n_total is None else n_total
         self.K, self.L, self.n_sink = K, L, n_sink
         self.W = _f64(W)
-        self.center = center_of_keys(keys, n_sink, n_prefill)
+        # centering=False is the pages' ablation without the data pre-processing step:
+        # keys are hashed as they are (c = 0), and p uses cos(q, k)
+        self.center = center_of_keys(keys, n_sink, n_prefill) if centering else np.zeros(keys.shape[1])
         self.codes = simhash_codes(keys[:n_total], self.W, K, L, self.center)
         self.ties = near_ties(keys[:n_total], self.W, self.center)
 

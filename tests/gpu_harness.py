@@ -10,20 +10,21 @@ import oracle as O
 import workloads as WL
 
 
-def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0):
+def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0, centering: bool = True):
     return mp.make_config(layers=wl.layers, batch=wl.batch, kv_heads=wl.kv_heads, q_heads=wl.q_heads,
                           head_dim=wl.head_dim, K=wl.K, L=wl.L, n_sink=wl.n_sink, window=wl.window,
                           capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer,
-                          threshold=threshold, match_mode=match_mode)
+                          threshold=threshold, match_mode=match_mode, centering=centering)
 
 
 class GpuRun:
     """Buffers and calls for one workload on one device."""
 
-    def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2, match_mode: int = 0):
+    def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2, match_mode: int = 0,
+                 centering: bool = True):
         self.mp, self.wl, self.dev = mp, wl, torch.device(device)
         self.threshold = threshold
-        self.cfg = config_for(mp, wl, threshold, match_mode)
+        self.cfg = config_for(mp, wl, threshold, match_mode, centering)
         self.tl = mp.mp_tables_layout_get(self.cfg)
         self.dl = mp.mp_decode_layout_get(self.cfg)
         self.tables = torch.empty(self.tl.total_bytes, dtype=torch.uint8, device=self.dev)
@@ -185,10 +186,10 @@ def check_planes(planes: np.ndarray, codes: np.ndarray, n: int, K: int) -> None:
 
 def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshold: int = 2,
                    units=None, qheads=None, steps=None, check_csr_tables: int = 8, tol: float = 2e-3,
-                   match_mode: int = 0) -> dict:
+                   match_mode: int = 0, centering: bool = True) -> dict:
     """Build, append and decode `wl` through the C ABI and compare every stage with the
     oracle on the chosen units / query heads / steps. Returns counters for reporting."""
-    run = GpuRun(mp, wl, tensors, device, threshold, match_mode)
+    run = GpuRun(mp, wl, tensors, device, threshold, match_mode, centering)
     run.build()
     torch.cuda.synchronize()
     assert run.status() == 0, hex(run.status())
@@ -205,7 +206,7 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
         u = unit_index(wl, l, b, h)
         k64 = tensors["keys"][l, b, h, :n_tot].double().cpu().numpy()
         W64 = tensors["W"][l if wl.w_per_layer else 0].double().cpu().numpy()
-        tab = O.HeadTables(k64, W64, wl.K, wl.L, wl.n_sink, wl.n_prefill, n_total=n_tot)
+        tab = O.HeadTables(k64, W64, wl.K, wl.L, wl.n_sink, wl.n_prefill, n_total=n_tot, centering=centering)
         oracle_tabs[u] = tab
         tiec = tie_codes(tab.ties, wl.K, wl.L)
         n0 = wl.n_prefill

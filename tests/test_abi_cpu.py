@@ -60,6 +60,10 @@ def test_config_validation(mp):
     c = _cfg(mp)
     c.reserved[2] = 1
     assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
+    assert mp.mp_config_check(_cfg(mp, centering=False)) == mp.MP_OK
+    c = _cfg(mp)
+    c.no_centering = 2
+    assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
 
 
 def test_layouts_are_aligned_disjoint_and_sized(mp):

@@ -67,6 +67,20 @@ def test_dtypes_and_head_dims(mp, kw):
     _report(str(kw), rep)
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+def test_centering_off(mp, mode):
+    """The pages' centering ablation: keys hashed as they are (c = 0), p from cos(q, k),
+    in both match modes; the cone-shaped keys then give a different sampled budget."""
+    wl = WL.Workload("nocenter", layers=1, batch=1, kv_heads=2, q_heads=8, head_dim=128, n_prefill=6000,
+                     steps=3, append=True, K=8, L=60, dtype="bf16", seed=77)
+    t = WL.generate(wl)
+    off = check_workload(mp, wl, t, match_mode=mode, centering=False, check_csr_tables=wl.L)
+    _report("centering off", off)
+    on = check_workload(mp, wl, t, match_mode=mode, check_csr_tables=4)
+    _report("centering on", on)
+    assert off["sampled"] != on["sampled"]
+
+
 @pytest.mark.parametrize("threshold,mode", [(1, 1), (1, 2), (3, 1), (3, 2), (5, 1), (7, 2)])
 def test_thresholds(mp, threshold, mode):
     """u = P[Bin(L, p^K) >= T] and the sampling rule for T other than the pages' 2

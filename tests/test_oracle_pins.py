@@ -305,3 +305,22 @@ def test_translation_of_all_keys_changes_nothing():
     assert len(a["S"]) > 0
     np.testing.assert_allclose(a["u"], b["u"], rtol=1e-10)
     np.testing.assert_allclose(a["out"], b["out"], rtol=1e-9)
+
+
+def test_centering_off_hashes_raw_keys_and_is_not_translation_invariant():
+    """The centering ablation (c = 0): codes are the SimHash of the raw keys, so shifting
+    every key by a vector changes them, while with centering the shift cancels
+    (§4.3 "Data pre-processing": the center removes the common component)."""
+    rng = np.random.default_rng(11)
+    d, K, L, s, n0 = 16, 4, 6, 2, 300
+    keys = rng.standard_normal((n0, d))
+    W = rng.standard_normal((d, K * L))
+    shift = 5.0 * rng.standard_normal(d)
+    off = O.HeadTables(keys, W, K, L, s, n0, centering=False)
+    assert np.all(off.center == 0)
+    np.testing.assert_array_equal(off.codes, O.simhash_codes(keys, W, K, L))
+    on_a = O.HeadTables(keys, W, K, L, s, n0)
+    on_b = O.HeadTables(keys + shift, W, K, L, s, n0)
+    np.testing.assert_array_equal(on_a.codes, on_b.codes)
+    off_b = O.HeadTables(keys + shift, W, K, L, s, n0, centering=False)
+    assert np.any(off_b.codes != off.codes)
