@@ -62,7 +62,9 @@ extern "C" {
 #define MP_ERR_SCRATCH (-6)     /* scratch buffer smaller than required */
 
 /* device status bits (mp_get_status) */
-#define MP_STATUS_W_NOT_BF16 0x1u   /* bf16 path: a W entry was not bf16-representable */
+#define MP_STATUS_W_NOT_BF16 0x1u   /* informational, bf16 configs: W is not bf16-representable, so the
+                                       tensor-core hashing runs on its three-term bf16 split (three
+                                       times the MMA work; results as exact as with fp32 W) */
 #define MP_STATUS_WAIT_TIMEOUT 0x2u /* a bounded wait on an mbarrier gave up */
 #define MP_STATUS_APPEND_GAP 0x4u   /* decode needed codes of a token never appended */
 #define MP_STATUS_NOT_BUILT 0x8u    /* decode or append on tables that were never built */
@@ -114,7 +116,9 @@ typedef struct mp_tables_layout {
   uint64_t negbeta_f32;  /* float [U][TC]: -W^T·center in tile-aligned column order (centering of
                             appended keys hashed on the tensor cores) */
   uint64_t wt_f32;       /* float [layers or 1][TC][d]: W transposed, tile-aligned column order */
-  uint64_t wt_bf16;      /* bf16  [layers or 1][TC][d]: the same in bf16 (bf16 configs only, else 0) */
+  uint64_t wt_bf16;      /* bf16  [layers or 1][3][TC][d] (bf16 configs only, else 0): W split into
+                            three bf16 terms hi, mid, lo with hi + mid + lo = W exactly (mid and lo
+                            are zero when W is bf16-representable) */
   uint64_t center_parts; /* float [U][parts][d]: partial sums while building */
   uint64_t codes;        /* uint16 [U][L][capacity]: code of every hashed token, table-major */
   uint64_t csr_offsets;  /* uint16 [U][L][NB+1][NS]: per table, bucket b and 32768-token segment s of

@@ -109,7 +109,7 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
   off = align256(off + uint64_t(g.n_w) * g.kltc * d * 4);
   if (g.dtype == MP_DTYPE_BF16) {
     o->wt_bf16 = off;
-    off = align256(off + uint64_t(g.n_w) * g.kltc * d * 2);
+    off = align256(off + uint64_t(g.n_w) * 3 * g.kltc * d * 2);
   }
   o->center_parts = off;
   off = align256(off + U * uint64_t(g.parts) * d * 4);
@@ -380,7 +380,7 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
     a.center = t.center;
     a.c_gs = 1;
     a.c_rs = 0;
-    a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+    a.wt = t.wt32;
     a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
     a.groups_per_w = g.batch * g.kvh;
     a.out = t.codes;
@@ -422,7 +422,7 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   a.center = t.center;
   a.c_gs = g.batch * g.kvh;
   a.c_rs = 1;
-  a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+  a.wt = t.wt32;
   a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
   a.out = t.codes;
@@ -498,7 +498,7 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   a.groups = g.layers;
   a.row0 = 0;
   a.center = nullptr;
-  a.wt = g.dtype == MP_DTYPE_BF16 ? static_cast<const void*>(t.wt16) : static_cast<const void*>(t.wt32);
+  a.wt = t.wt32;
   a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
   a.out = dp.qcodes;

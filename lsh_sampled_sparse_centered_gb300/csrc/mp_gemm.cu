@@ -203,10 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   GemmSmem<D>& S = *reinterpret_cast<GemmSmem<D>*>(smraw + ((1024 - (base & 1023)) & 1023));
   constexpr int kSub = GemmSmem<D>::kSub;
   constexpr uint32_t kABytes = kTileM * D * 2;
-  constexpr uint32_t kBBytes = kTileN * D * 2 + kTileN * 16 * 2;  // W columns + their -beta split
+  constexpr uint32_t kWBytes = kTileN * D * 2;                    // one bf16 term of the W columns
+  constexpr uint32_t kBBytes = kWBytes + kTileN * 16 * 2;         // + their -beta split (first term)
   constexpr uint32_t kOnesBytes = kTileM * 16 * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (n0 + kTileM - 1) / kTileM;
+  // bf16 terms of W to accumulate: 1, or 3 (hi, mid, lo) when W is not bf16-representable
+  const int terms = hdr->w_terms3 ? 3 : 1;
   const int items = units * mt;
   volatile uint32_t* abort = &S.abort;
 
@@ -247,18 +250,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&S.a_empty[as], ((li >> 1) & 1) ^ 1, abort)) break;
         mbar_expect_tx(&S.a_full[as], kABytes);
         for (int s = 0; s < kSub; ++s) tma_load_2d(&S.a[as][s][0], &tmK, s * 64, u * cap + m0, &S.a_full[as]);
-        const int wrow = (w_per_layer ? (u / units_per_w) : 0) * nt * kTileN;
+        const int wrow = (w_per_layer ? (u / units_per_w) : 0) * 3 * kltc;  // [n_w][3][kltc] rows
         bool ok = true;
-        for (int n = 0; n < nt; ++n, ++bc) {
-          const int bs = bc & 1;
-          if (!mbar_wait(&S.b_empty[bs], ((bc >> 1) & 1) ^ 1, abort)) {
-            ok = false;
-            break;
+        for (int n = 0; n < nt && ok; ++n) {
+          for (int j = 0; j < terms; ++j, ++bc) {
+            const int bs = bc & 1;
+            if (!mbar_wait(&S.b_empty[bs], ((bc >> 1) & 1) ^ 1, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&S.b_full[bs], j == 0 ? kBBytes : kWBytes);
+            for (int s = 0; s < kSub; ++s)
+              tma_load_2d(&S.b[bs][s][0], &tmW, s * 64, wrow + j * kltc + n * kTileN, &S.b_full[bs]);
+            if (j == 0) tma_load_2d(&S.b1[bs][0], &tmBias, 0, u * kltc + n * kTileN, &S.b_full[bs]);
           }
-          mbar_expect_tx(&S.b_full[bs], kBBytes);
-          for (int s = 0; s < kSub; ++s)
-            tma_load_2d(&S.b[bs][s][0], &tmW, s * 64, wrow + n * kTileN, &S.b_full[bs]);
-          tma_load_2d(&S.b1[bs][0], &tmBias, 0, u * kltc + n * kTileN, &S.b_full[bs]);
         }
         if (!ok) break;
       }
@@ -276,25 +281,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&S.a_full[as], (li >> 1) & 1, abort)) break;
         fence_after();
         bool ok = true;
-        for (int n = 0; n < nt; ++n, ++bc, ++ac) {
-          const int bs = bc & 1, cs = ac & 1;
-          if (!mbar_wait(&S.b_full[bs], (bc >> 1) & 1, abort) ||
-              !mbar_wait(&S.acc_empty[cs], ((ac >> 1) & 1) ^ 1, abort)) {
+        for (int n = 0; n < nt && ok; ++n, ++ac) {
+          const int cs = ac & 1;
+          if (!mbar_wait(&S.acc_empty[cs], ((ac >> 1) & 1) ^ 1, abort)) {
             ok = false;
             break;
           }
-          fence_after();
           const uint32_t d_tmem = tmem + uint32_t(cs * kTileN);
+          for (int j = 0; j < terms; ++j, ++bc) {
+            const int bs = bc & 1;
+            if (!mbar_wait(&S.b_full[bs], (bc >> 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int s = kk >> 2, off = (kk & 3) * 32;
-            const uint64_t da = sw128_desc(saddr(&S.a[as][s][0]) + off);
-            const uint64_t db = sw128_desc(saddr(&S.b[bs][s][0]) + off);
-            mma_bf16(d_tmem, da, db, idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int s = kk >> 2, off = (kk & 3) * 32;
+              const uint64_t da = sw128_desc(saddr(&S.a[as][s][0]) + off);
+              const uint64_t db = sw128_desc(saddr(&S.b[bs][s][0]) + off);
+              mma_bf16(d_tmem, da, db, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            // extra K step (with the first term): ones x (-beta split) adds -W^T c to every row
+            if (j == 0) mma_bf16(d_tmem, sw32_desc(saddr(&S.a1[0])), sw32_desc(saddr(&S.b1[bs][0])), idesc, 1u);
+            mma_commit(&S.b_empty[bs]);
           }
-          // extra K step: ones x (-beta split) adds -W^T c to every row
-          mma_bf16(d_tmem, sw32_desc(saddr(&S.a1[0])), sw32_desc(saddr(&S.b1[bs][0])), idesc, 1u);
-          mma_commit(&S.b_empty[bs]);
+          if (!ok) break;
           mma_commit(&S.acc_full[cs]);
         }
         if (!ok) break;
@@ -398,7 +410,7 @@ struct RowsLayout {
   }
   __host__ __device__ static constexpr uint32_t bits_off(int nr) { return b_off(kSub, nr); }
   __host__ __device__ static constexpr uint32_t ctl_off(int nr) { return bits_off(nr) + uint32_t(nr) * 9u * 4u; }
-  __host__ __device__ static constexpr uint32_t bytes(int nr) { return ctl_off(nr) + 64u; }
+  __host__ __device__ static constexpr uint32_t bytes(int nr) { return ctl_off(nr) + 64u; }  // 3 barriers + slots
 };
 
 struct RowsTcArgs {
@@ -427,7 +439,8 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   uint32_t* bits = reinterpret_cast<uint32_t*>(sm + Lay::bits_off(nr));  // [nr][9]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lay::ctl_off(nr));
   uint64_t* accb = full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  uint64_t* mdone = full + 2;  // the MMAs of one W term have read the A tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 3);
   volatile uint32_t* abort = tmem_slot + 1;
   const int g = blockIdx.z, n = blockIdx.y, rb = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -439,6 +452,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   if (threadIdx.x == 0) {
     mbar_init(full, 1);
     mbar_init(accb, 1);
+    mbar_init(mdone, 1);
     *abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (a.negbeta && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
@@ -459,18 +473,23 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   const uint32_t tmem = *tmem_slot;
 
   if (threadIdx.x == 0) {
+    // W terms (1, or hi, mid, lo when W is not bf16-representable) go through the one A
+    // buffer in turn; the rows are loaded with the first term
+    const int terms = a.hdr->w_terms3 ? 3 : 1;
     const int wrow = (g / a.groups_per_w) * a.w_rows + n * 256;
     const int xrow = g * a.rows + r0;
-    mbar_expect_tx(full, uint32_t(kSub) * (Lay::kABytes + uint32_t(nr) * 128u));
-    for (int s = 0; s < kSub; ++s) {
-      tma_load_2d(sm + Lay::a_off(s), &tmW, s * 64, wrow, full);
-      tma_load_2d(sm + Lay::b_off(s, nr), &tmX, s * 64, xrow, full);
-    }
-    if (mbar_wait(full, 0, abort)) {
+    // D[col][row]: M = 128 W columns per half, N = nr rows
+    const uint32_t idesc =
+        (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nr >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    for (int j = 0; j < terms; ++j) {
+      if (j > 0 && !mbar_wait(mdone, (j - 1) & 1, abort)) break;
+      mbar_expect_tx(full, uint32_t(kSub) * (Lay::kABytes + (j == 0 ? uint32_t(nr) * 128u : 0u)));
+      for (int s = 0; s < kSub; ++s) {
+        tma_load_2d(sm + Lay::a_off(s), &tmW, s * 64, wrow + j * a.kltc, full);
+        if (j == 0) tma_load_2d(sm + Lay::b_off(s, nr), &tmX, s * 64, xrow, full);
+      }
+      if (!mbar_wait(full, j & 1, abort)) break;
       fence_after();
-      // D[col][row]: M = 128 W columns per half, N = nr rows
-      const uint32_t idesc =
-          (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nr >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -478,9 +497,9 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
           const int s = kk >> 2, off = (kk & 3) * 32;
           const uint64_t da = sw128_desc(saddr(sm + Lay::a_off(s)) + uint32_t(h) * 16384u + off);
           const uint64_t db = sw128_desc(saddr(sm + Lay::b_off(s, nr)) + off);
-          mma_bf16(tmem + uint32_t(h * nr), da, db, idesc, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + uint32_t(h * nr), da, db, idesc, (j > 0 || kk > 0) ? 1u : 0u);
         }
-      mma_commit(accb);
+      mma_commit(j + 1 < terms ? mdone : accb);
     }
   }
   __syncwarp();
@@ -580,7 +599,7 @@ template <int D, int KT>
 cudaError_t launch_tc(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t, cudaStream_t st) {
   CUtensorMap mk, mw, mb, mo;
   if (!make_map(&mk, keys, uint64_t(g.d), uint64_t(g.units) * g.cap, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mw, t.wt16, uint64_t(g.d), uint64_t(g.n_w) * g.kltc, 64, kTileN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&mw, t.wt16, uint64_t(g.d), uint64_t(g.n_w) * 3 * g.kltc, 64, kTileN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mb, t.beta, 16, uint64_t(g.units) * g.kltc, 16, kTileN, CU_TENSOR_MAP_SWIZZLE_32B) ||
       !make_map(&mo, t.ones, 16, kTileM, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
@@ -602,7 +621,7 @@ cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t 
   a.rows = h.rows;
   a.nr = std::min(256, (h.rows + 31) / 32 * 32);
   a.groups_per_w = h.groups_per_w;
-  a.w_rows = g.w_per_layer ? g.kltc : 0;
+  a.w_rows = g.w_per_layer ? 3 * g.kltc : 0;
   a.negbeta = h.negbeta;
   a.kltc = g.kltc;
   a.out = h.out;
@@ -612,7 +631,7 @@ cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t 
   a.hdr = h.hdr;
   a.mark_pos = h.mark_pos;
   CUtensorMap mw, mx;
-  if (!make_map(&mw, h.wt16, uint64_t(g.d), uint64_t(g.n_w) * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!make_map(&mw, h.wt16, uint64_t(g.d), uint64_t(g.n_w) * 3 * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_strided(&mx, h.x, uint64_t(g.d), uint64_t(h.rows) * h.groups, uint64_t(h.x_rs) * 2, 64,
                         uint32_t(a.nr), CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;

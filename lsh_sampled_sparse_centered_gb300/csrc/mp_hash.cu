@@ -10,13 +10,17 @@
 namespace mp {
 
 // ---------------------------------------------------------------------------------
-// W [n_w][d][K*L] fp32 -> wt32 [n_w][TC][d] fp32 and (bf16 configs) wt16 [n_w][TC][d]
+// W [n_w][d][K*L] fp32 -> wt32 [n_w][TC][d] fp32 and (bf16 configs) wt16 [n_w][3][TC][d]
 // in tile-aligned column order: 256-column tile n holds tables n*tpt .. n*tpt+tpt-1,
 // column n*256 + i*K + b is bit b of the tile's i-th table; the other columns are zero.
+// wt16 holds W as three bf16 terms: hi = bf16(W), mid = bf16(W - hi), lo = bf16(W - hi -
+// mid); each step removes at least 8 mantissa bits, so hi + mid + lo = W exactly. If any
+// mid or lo term is nonzero the header's w_terms3 flag (and the informational status
+// bit) tells the tensor-core kernels to add the two extra terms.
 // ---------------------------------------------------------------------------------
 __global__ void k_prepare_w(const float* __restrict__ W, float* __restrict__ wt32,
                             __nv_bfloat16* __restrict__ wt16, int d, int K, int L, int tpt, int kltc,
-                            uint32_t* status) {
+                            DevHeader* hdr) {
   const int m = blockIdx.y;
   const int jc = blockIdx.x;  // one tensor-core column per block, d threads
   const int kl = K * L;
@@ -27,21 +31,29 @@ __global__ void k_prepare_w(const float* __restrict__ W, float* __restrict__ wt3
   bool inexact = false;
   for (int dd = threadIdx.x; dd < d; dd += blockDim.x) {
     const float v = live ? W[(int64_t(m) * d + dd) * kl + t * K + b] : 0.f;
-    const int64_t o = (int64_t(m) * kltc + jc) * d + dd;
-    wt32[o] = v;
+    wt32[(int64_t(m) * kltc + jc) * d + dd] = v;
     if (wt16) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(v);
-      wt16[o] = h;
-      inexact |= (__bfloat162float(h) != v);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const float r1 = v - __bfloat162float(hi);
+      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+      const int64_t o = ((int64_t(m) * 3) * kltc + jc) * d + dd;
+      wt16[o] = hi;
+      wt16[o + int64_t(kltc) * d] = mid;
+      wt16[o + 2 * int64_t(kltc) * d] = lo;
+      inexact |= (r1 != 0.f);
     }
   }
-  if (inexact) atomicOr(status, MP_STATUS_W_NOT_BF16);
+  if (inexact) {
+    atomicOr(&hdr->status, MP_STATUS_W_NOT_BF16);
+    atomicOr(&hdr->w_terms3, 1u);
+  }
 }
 
 cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st) {
   if (g.kltc == 0) return cudaSuccess;
   dim3 grid(g.kltc, g.n_w);
-  k_prepare_w<<<grid, 128, 0, st>>>(W, t.wt32, t.wt16, g.d, g.K, g.L, g.tpt, g.kltc, &t.hdr->status);
+  k_prepare_w<<<grid, 128, 0, st>>>(W, t.wt32, t.wt16, g.d, g.K, g.L, g.tpt, g.kltc, t.hdr);
   return cudaGetLastError();
 }
 
@@ -105,7 +117,7 @@ __global__ void __launch_bounds__(256) k_center_parts(const T* __restrict__ keys
 __global__ void k_center_final(const float* __restrict__ cparts, float* __restrict__ center,
                                __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ ones,
                                float* __restrict__ negbeta,
-                               const __nv_bfloat16* __restrict__ wt16, int d,
+                               const float* __restrict__ wt32, int tc, int d,
                                int kltc, int parts, int count, int units_per_w, int64_t w_stride,
                                DevHeader* hdr, int n_prefill, int no_center) {
   extern __shared__ float c[];  // [d]
@@ -118,15 +130,15 @@ __global__ void k_center_final(const float* __restrict__ cparts, float* __restri
     center[int64_t(u) * d + dim] = v;
   }
   __syncthreads();
-  // -beta = -W^T c in tensor-core column order as three bf16 terms hi + mid + lo (each
-  // the bf16 rounding of what is left), an exact split of the fp32 value: the
+  // -beta = -W^T c (fp32 W) in tensor-core column order as three bf16 terms hi + mid + lo
+  // (each the bf16 rounding of what is left), an exact split of the fp32 value: the
   // tensor-core hash adds them through one extra K step against rows of ones
-  if (wt16) {
-    const __nv_bfloat16* w = wt16 + int64_t(u / units_per_w) * w_stride;
+  if (tc) {
+    const float* w = wt32 + int64_t(u / units_per_w) * w_stride;
     for (int j = threadIdx.x; j < kltc; j += blockDim.x) {
-      const __nv_bfloat16* row = w + int64_t(j) * d;
+      const float* row = w + int64_t(j) * d;
       float sacc = 0.f;
-      for (int dim = 0; dim < d; ++dim) sacc = fmaf(__bfloat162float(row[dim]), c[dim], sacc);
+      for (int dim = 0; dim < d; ++dim) sacc = fmaf(row[dim], c[dim], sacc);
       const float nb = -sacc;
       negbeta[int64_t(u) * kltc + j] = nb;
       const __nv_bfloat16 hi = __float2bfloat16_rn(nb);
@@ -166,7 +178,8 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
-  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.negbeta, t.wt16, g.d,
+  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.negbeta, t.wt32,
+                                                          t.wt16 != nullptr, g.d,
                                                           g.kltc, g.parts, hi - lo, g.batch * g.kvh,
                                                           w_stride, t.hdr, n_prefill, g.no_center);
   return cudaGetLastError();
@@ -290,8 +303,9 @@ static void launch_rows_tw(const Geometry& g, const HashRowsArgs& a, cudaStream_
 
 template <int R>
 static void launch_rows_t(const Geometry& g, const HashRowsArgs& a, cudaStream_t st) {
-  // bf16 configs hash with the bf16 copy of W (the values the tensor cores use)
-  if (g.dtype == MP_DTYPE_BF16) launch_rows_tw<__nv_bfloat16, __nv_bfloat16, R>(g, a, st);
+  // the fp32 W, exact for any W (the tensor-core paths reach the same values through
+  // W's three-term bf16 split)
+  if (g.dtype == MP_DTYPE_BF16) launch_rows_tw<__nv_bfloat16, float, R>(g, a, st);
   else launch_rows_tw<float, float, R>(g, a, st);
 }
 

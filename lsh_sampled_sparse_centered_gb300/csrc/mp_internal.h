@@ -24,7 +24,9 @@ struct DevHeader {
   int32_t n_prefill;     // tokens hashed at build time
   int32_t appended_end;  // one past the last token whose code is stored
   uint32_t status;       // MP_STATUS_* bits
-  int32_t pad[60];
+  uint32_t w_terms3;     // nonzero: W is not bf16-representable, the tensor-core paths add
+                         // the mid and lo bf16 terms of the split W = hi + mid + lo
+  int32_t pad[59];
 };
 static_assert(sizeof(DevHeader) == 256, "header size");
 
@@ -54,7 +56,7 @@ struct TablesPtrs {
   __nv_bfloat16* ones;   // [128][16]: (1, 1, 1, 0, ...) per row
   float* negbeta;        // [U][kltc]: -W^T c
   float* wt32;
-  __nv_bfloat16* wt16;
+  __nv_bfloat16* wt16;   // [n_w][3][kltc][d]: hi, mid, lo bf16 terms of W (W = hi + mid + lo)
   float* cparts;
   uint16_t* codes;
   uint16_t* off;   // [U][L][nseg][nb+1]

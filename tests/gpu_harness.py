@@ -192,7 +192,8 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
     run = GpuRun(mp, wl, tensors, device, threshold, match_mode, centering)
     run.build()
     torch.cuda.synchronize()
-    assert run.status() == 0, hex(run.status())
+    # the W status bit is informational (the tensor-core paths then use W's three-term split)
+    assert (run.status() & ~mp.MP_STATUS_W_NOT_BF16) == 0, hex(run.status())
     U = wl.layers * wl.batch * wl.kv_heads
     all_units = [(l, b, h) for l in range(wl.layers) for b in range(wl.batch) for h in range(wl.kv_heads)]
     units = all_units if units is None else units
@@ -237,7 +238,7 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
         out = out_t.cpu().numpy()
         torch.cuda.synchronize()
         st = run.status()
-        assert st == 0, hex(st)
+        assert (st & ~mp.MP_STATUS_W_NOT_BF16) == 0, hex(st)
         qc, ln, ns = run.decode_state()
         for (l, b, h) in units:
             u = unit_index(wl, l, b, h)

@@ -58,6 +58,8 @@ def test_ragged_appends_leave_the_window(mp):
 @pytest.mark.parametrize("kw", [
     dict(dtype="f32", head_dim=128, w_bf16=False),
     dict(dtype="bf16", head_dim=64),
+    dict(dtype="bf16", head_dim=128, w_bf16=False),   # fp32 W: three-term bf16 split on the tensor cores
+    dict(dtype="bf16", head_dim=64, w_bf16=False),
     dict(dtype="f32", head_dim=64, q_heads=2, kv_heads=2, w_bf16=False),
 ])
 def test_dtypes_and_head_dims(mp, kw):
