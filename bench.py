@@ -345,7 +345,7 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic: seeded cone keys k=3mu+N(0,I) with sink k0=-6mu, queries q=-2mu+N(0,I), "
-                "values N(0,1), W N(0,1) rounded to bf16",
+                "values N(0,1), W N(0,1)" + (" rounded to bf16" if wl.w_bf16 else " in fp32"),
         "config": {"workload": wl.name, "layers": wl.layers, "batch": wl.batch, "kv_heads": wl.kv_heads,
                    "q_heads": wl.q_heads, "head_dim": wl.head_dim, "n_prefill": wl.n_prefill,
                    "decode_steps": wl.steps, "K": wl.K, "L": wl.L, "n_sink": wl.n_sink, "window": wl.window,
