@@ -479,13 +479,35 @@ def run_e2e(job, stream, args, world):
     torch.cuda.synchronize()
 
     graph, job.graph = job.graph, None
+    # host -> device copies in 256 MB pieces spread over eight copy streams (the host
+    # link takes several copies at once); the build waits for the keys and W only, so
+    # the values' copy overlaps it, and the decode steps wait for the values
+    copy_streams = [torch.cuda.Stream(device=job.dev) for _ in range(8)]
+    piece = 256 << 20
+
+    def h2d(dst, src, events):
+        d, h = dst.view(-1).view(torch.uint8), src.view(-1).view(torch.uint8)
+        for i, o in enumerate(range(0, d.numel(), piece)):
+            cs = copy_streams[i % len(copy_streams)]
+            with torch.cuda.stream(cs):
+                d[o: o + piece].copy_(h[o: o + piece], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                events.append(ev)
 
     def one():
-        d_keys.copy_(h_keys, non_blocking=True)
-        d_vals.copy_(h_vals, non_blocking=True)
-        d_W.copy_(h_W, non_blocking=True)
-        d_q.copy_(h_q, non_blocking=True)
+        for cs in copy_streams:
+            cs.wait_stream(stream)  # previous job done with the device buffers
+        ev_build, ev_decode = [], []
+        h2d(d_keys, h_keys, ev_build)
+        h2d(d_W, h_W, ev_build)
+        h2d(d_q, h_q, ev_decode)
+        h2d(d_vals, h_vals, ev_decode)
+        for ev in ev_build:
+            stream.wait_event(ev)
         job.build(keys=d_keys, W=d_W)
+        for ev in ev_decode:
+            stream.wait_event(ev)
         job.decode_steps(keys=d_keys, values=d_vals, queries=d_q)
         h_out.copy_(job.outs, non_blocking=True)
 
