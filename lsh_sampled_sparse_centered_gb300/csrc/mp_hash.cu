@@ -187,22 +187,18 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
 
 // ---------------------------------------------------------------------------------
 // SimHash of rows on CUDA cores: a CTA hashes R rows against one 256-column tile of
-// W (whole tables, tile-aligned order). The W tile (bf16 for bf16 configs, fp32
-// otherwise) is copied into shared memory with 16-byte loads, rows padded to an odd
+// W (whole tables, tile-aligned order). The fp32 W tile
+// is copied into shared memory with 16-byte loads, rows padded to an odd
 // number of words so that thread j reading column j hits distinct banks. Thread j
 // keeps the R projections of column j in registers; a warp ballot per row turns the
 // signs into bits and the bits are cut into K-bit codes.
 // ---------------------------------------------------------------------------------
 constexpr int kHashCols = 256;
 
-// four consecutive W elements of a shared-memory row as two packed fp32 pairs
+// four consecutive fp32 W elements of a shared-memory row as two packed pairs
 __device__ __forceinline__ void w4(const float* p, uint64_t& a, uint64_t& b) {
   a = pk2(p[0], p[1]);
   b = pk2(p[2], p[3]);
-}
-__device__ __forceinline__ void w4(const __nv_bfloat16* p, uint64_t& a, uint64_t& b) {
-  a = bf2_to_f2(*reinterpret_cast<const uint32_t*>(p));
-  b = bf2_to_f2(*reinterpret_cast<const uint32_t*>(p + 2));
 }
 
 template <typename T, typename WT, int R>

@@ -142,13 +142,14 @@ def test_status_flags(mp):
     assert run.status() == mp.MP_STATUS_APPEND_GAP
 
 
-@pytest.mark.parametrize("path", ["simt", "tc"])
-def test_both_key_hash_paths_match_the_oracle(mp, path, monkeypatch):
-    """Prefill keys are hashed on tensor cores (default) or on CUDA cores
-    (MP_HASH_PATH=simt); both must give the oracle's codes except near ties."""
+@pytest.mark.parametrize("path,w_bf16", [("simt", True), ("tc", True), ("simt", False), ("tc", False)])
+def test_both_key_hash_paths_match_the_oracle(mp, path, w_bf16, monkeypatch):
+    """Keys, queries and appended keys are hashed on tensor cores (default) or on CUDA
+    cores (MP_HASH_PATH=simt); both must give the oracle's codes except near ties, with
+    one W per layer, bf16-representable or not (three-term split on the tensor cores)."""
     monkeypatch.setenv("MP_HASH_PATH", path)
-    wl = WL.Workload("paths", layers=2, batch=1, kv_heads=2, q_heads=4, head_dim=128, n_prefill=4099, steps=1,
-                     append=False, K=10, L=50, dtype="bf16", seed=41, w_per_layer=True)
+    wl = WL.Workload("paths", layers=2, batch=1, kv_heads=2, q_heads=4, head_dim=128, n_prefill=4099, steps=2,
+                     append=True, K=10, L=50, dtype="bf16", seed=41, w_per_layer=True, w_bf16=w_bf16)
     rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=50)
     _report(f"hash path {path}", rep)
 
