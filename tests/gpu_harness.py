@@ -17,7 +17,7 @@ def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0, cen
                           threshold=threshold, match_mode=match_mode, centering=centering)
 
 
-class GpuRun:
+class DeviceRun:
     """Buffers and calls for one workload on one device."""
 
     def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2, match_mode: int = 0,
@@ -189,7 +189,7 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
                    match_mode: int = 0, centering: bool = True) -> dict:
     """Build, append and decode `wl` through the C ABI and compare every stage with the
     oracle on the chosen units / query heads / steps. Returns counters for reporting."""
-    run = GpuRun(mp, wl, tensors, device, threshold, match_mode, centering)
+    run = DeviceRun(mp, wl, tensors, device, threshold, match_mode, centering)
     run.build()
     torch.cuda.synchronize()
     # the W status bit is informational (the tensor-core paths then use W's three-term split)

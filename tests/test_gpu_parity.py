@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import workloads as WL
-from gpu_harness import GpuRun, check_workload, config_for, rel_l2
+from gpu_harness import DeviceRun, check_workload, config_for, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -101,7 +101,7 @@ def test_K0_samples_everything_and_equals_exact_attention(mp):
     t = WL.generate(wl)
     rep = check_workload(mp, wl, t)
     assert rep["sampled"] == rep["region"]
-    run = GpuRun(mp, wl, t, "cuda:0")
+    run = DeviceRun(mp, wl, t, "cuda:0")
     run.build()
     out = run.decode(0, 700).cpu().numpy()
     k = t["keys"][0, 0, 0].double().numpy()
@@ -124,7 +124,7 @@ def test_status_flags(mp):
     wl = WL.Workload("st", layers=1, batch=1, kv_heads=1, q_heads=1, head_dim=128, n_prefill=300, steps=100,
                      append=True, K=4, L=4, dtype="bf16", seed=3, window=8)
     t = WL.generate(wl)
-    run = GpuRun(mp, wl, t, "cuda:0")
+    run = DeviceRun(mp, wl, t, "cuda:0")
     # decode on never-built tables
     run.tables.zero_()
     run.decode(0, 300)

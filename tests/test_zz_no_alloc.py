@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads as WL
-from gpu_harness import GpuRun, rel_l2
+from gpu_harness import DeviceRun, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ def mp():
 
 def test_static_scratch_decode_matches_the_scratch_buffer_decode(mp):
     wl = WL.WORKLOADS[1].replace(n_prefill=5000, steps=2, append=True)
-    run = GpuRun(mp, wl, WL.generate(wl), "cuda:0")
+    run = DeviceRun(mp, wl, WL.generate(wl), "cuda:0")
     assert mp.mp_decode_layout_get(run.cfg).total_bytes <= mp.MP_STATIC_SCRATCH_BYTES
     run.build()
     stream = torch.cuda.current_stream().cuda_stream
