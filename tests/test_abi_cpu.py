@@ -79,10 +79,16 @@ def test_layouts_are_aligned_disjoint_and_sized(mp):
     assert t.total_bytes - t.csr_ids >= U * L * cap * 2
     assert t.tc_cols == 768 and t.n_buckets == 256
     assert t.wt_bf16 - t.wt_f32 >= 2 * 768 * d * 4
+    assert t.center_parts - t.wt_bf16 >= 2 * 3 * 768 * d * 2      # hi, mid, lo bf16 terms of W
+    assert t.wt_f32 - t.negbeta_f32 >= U * 768 * 4                  # fp32 -beta per unit and column
+    assert t.negbeta_f32 - t.ones >= 128 * 16 * 2
+    assert t.ones - t.beta >= U * 768 * 16 * 2
+    ns = -(-cap // 32768)
+    assert t.csr_ids - t.csr_offsets >= U * L * (256 + 1) * ns * 2  # bucket-major offsets
     dl = mp.mp_decode_layout_get(c)
     Q = 2 * 4
     assert dl.lists % 256 == 0 and dl.partials - dl.lists >= Q * cap * 4
-    assert dl.total_bytes - dl.counters >= Q * 4
+    assert dl.total_bytes - dl.counters >= (Q + 1) * 4            # + the attention's work queue
     f32 = mp.mp_tables_layout_get(_cfg(mp, dtype="f32"))
     assert f32.wt_bf16 == 0
 
