@@ -4,15 +4,17 @@
  *
  * The method is the one of "MagicPIG: LSH Sampling for Efficient LLM Generation"
  * (arXiv 2410.16179v2):
- *   - keys are centered by their mean before hashing (§4.3 "Data pre-processing");
+ *   - keys are centered by their mean before hashing (§4.3 "Data pre-processing";
+ *     config.no_centering = 1 gives the pages' ablation without it);
  *   - each key and each query gets L SimHash codes of K bits from K·L random
  *     projections W ∈ R^{d×(K·L)} (§2.2 SimHash; §4.3 "Hash function selection";
  *     Algorithm 1 'Encode');
- *   - a key is sampled when its code equals the query's in at least two tables
- *     (§4.3; Algorithm 1 'Query');
+ *   - a key is sampled when its code equals the query's in at least T tables
+ *     (T = config.threshold; the pages take T = 2: §4.3; Algorithm 1 'Query');
  *   - the output is the self-normalised importance-sampling estimate
- *     softmax(q·k/√d − log u) V over the sampled keys, with
- *     u = 1 − (1 − p^K)^L − L p^K (1 − p^K)^(L−1), p = 1 − θ(q, k)/π (Eq. 9–11);
+ *     softmax(q·k/√d − log u) V over the sampled keys, with u = P[Bin(L, p^K) >= T]
+ *     (for T = 2: 1 − (1 − p^K)^L − L p^K (1 − p^K)^(L−1)) and p = 1 − θ(q, k − c)/π
+ *     (Eq. 9–11);
  *   - sink tokens and a local window are attended exactly with u = 1 (§4.4
  *     "On-device cache"; §5.1 Baselines: 4 sinks and a 64-token window).
  *
@@ -50,7 +52,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 1
+#define MP_ABI_VERSION 2 /* 2: mp_config.no_centering, mp_tables_layout.negbeta_f32, three-term W */
 
 /* return codes */
 #define MP_OK 0

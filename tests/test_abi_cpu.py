@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(mp):
     for n in names:
         assert getattr(lib, n) is not None
     assert set(mp.EXPORTED) <= set(names)
-    assert mp.mp_abi_version() == 1
+    assert mp.mp_abi_version() == 2
 
 
 def _cfg(mp, **kw):
