@@ -8,7 +8,12 @@
 // into three bf16 terms (exact). The epilogue keeps the sign of each projection and
 // packs K signs into each table's code (§2.2 SimHash, §4.3 "Hash function selection").
 // bf16 x bf16 products are exact in fp32, so with bf16-representable W the only
-// rounding is the fp32 accumulation.
+// rounding is the fp32 accumulation; a W that bf16 cannot hold enters as its exact
+// split hi + mid + lo, one pass of K steps per term into the same accumulator.
+//
+// The same file holds the swap-AB kernel that hashes the few rows of a decode step
+// (queries, appended keys): there the W columns are the M dimension, so a warp ballot
+// over tensor-memory lanes gives a row's sign bits directly.
 //
 // Structure: persistent CTAs, one per SM, each walking 128-key tiles. Warp 0 streams
 // key tiles (A, 128 x d) and W column tiles (B, 256 x d) with TMA into 128B-swizzled
