@@ -101,10 +101,17 @@ class MagicPigError(RuntimeError):
 
 
 def _ptr(x) -> Optional[int]:
+    """Device address of a tensor argument (ints pass through as raw addresses). The
+    kernels read and write these addresses directly, so a host tensor or a strided
+    view is refused here rather than handed to the GPU."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if getattr(x, "is_cuda", True) is False:
+        raise ValueError("tensor arguments must be CUDA tensors (device memory)")
+    if hasattr(x, "is_contiguous") and not x.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous (dense row-major layout)")
     return x.data_ptr()
 
 

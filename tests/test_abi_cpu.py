@@ -126,3 +126,14 @@ def test_fault_injection_on_the_host(mp, monkeypatch):
     with pytest.raises(mp.MagicPigError) as e:
         mp.mp_append(c, fake, fake, 20, stream=0)
     assert e.value.code == mp.MP_ERR_INJECTED
+
+
+def test_binding_refuses_host_and_strided_tensors(mp):
+    import pytest
+    import torch
+    c = _cfg(mp)
+    host = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        mp.mp_build_tables(c, host, 10, host, host, stream=0)
+    with pytest.raises(ValueError):
+        mp._ptr(torch.zeros(4, 4)[:, 1])
