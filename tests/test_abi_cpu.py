@@ -137,3 +137,16 @@ def test_binding_refuses_host_and_strided_tensors(mp):
         mp.mp_build_tables(c, host, 10, host, host, stream=0)
     with pytest.raises(ValueError):
         mp._ptr(torch.zeros(4, 4)[:, 1])
+
+
+def test_auto_match_mode_picks_the_fewer_bytes(mp):
+    """AUTO compares bytes per query head: the bucket walk reads L·m/2^K ids plus the
+    ranges; the bit-plane scan reads m·L·K/8 bytes shared by the G query heads of a
+    KV head. Long contexts with 4-head groups (the bench shape) walk buckets; a short
+    context with large groups and K = 1 streams the planes."""
+    big = _cfg(mp, kv_heads=8, q_heads=32, K=10, L=150, capacity=98368)
+    assert mp.mp_tables_layout_get(big).match_mode == mp.MP_MATCH_CSR
+    small = _cfg(mp, kv_heads=1, q_heads=64, K=1, L=8, capacity=2048)
+    assert mp.mp_tables_layout_get(small).match_mode == mp.MP_MATCH_SCAN
+    forced = _cfg(mp, kv_heads=1, q_heads=64, K=1, L=8, capacity=2048, match_mode=mp.MP_MATCH_CSR)
+    assert mp.mp_tables_layout_get(forced).match_mode == mp.MP_MATCH_CSR
