@@ -154,14 +154,29 @@ def test_both_key_hash_paths_match_the_oracle(mp, path, w_bf16, monkeypatch):
     _report(f"hash path {path}", rep)
 
 
-@pytest.mark.parametrize("K,L,d", [(9, 120, 128), (12, 40, 128), (7, 33, 64), (1, 5, 64)])
+@pytest.mark.parametrize("K,L,d", [(9, 120, 128), (12, 40, 128), (7, 33, 64), (1, 5, 64), (12, 1024, 128)])
 def test_tensor_core_hash_tile_layouts(mp, K, L, d):
     """Tables per 256-column tile = floor(256/K): K values that leave padding columns,
-    L not a multiple of it, both head dims."""
+    L not a multiple of it, both head dims; the largest K and L the library takes."""
     wl = WL.Workload(f"tc-{K}-{L}-{d}", layers=1, batch=1, kv_heads=1, q_heads=2, head_dim=d, n_prefill=700,
                      steps=1, append=False, K=K, L=L, dtype="bf16", seed=K * 100 + L)
     rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=L)
     _report(f"tc K={K} L={L} d={d}", rep)
+
+
+def test_maximum_capacity(mp):
+    """The largest capacity the library takes, 2^19 tokens, filled by the prefill up to
+    the two appended tokens: 16 bucketed segments per table (the last one ragged), the
+    match kernel's per-token bitmaps at their largest, and ~10^4 sampled keys per head
+    split across many attention slices."""
+    wl = WL.Workload("max-capacity", layers=1, batch=1, kv_heads=1, q_heads=4, head_dim=128,
+                     n_prefill=(1 << 19) - 2, steps=2, append=True, K=8, L=32, dtype="bf16", seed=19)
+    assert wl.capacity == 1 << 19
+    assert mp.mp_config_check(config_for(mp, wl)) == mp.MP_OK
+    assert mp.mp_config_check(config_for(mp, wl.replace(n_prefill=(1 << 19) - 1))) == mp.MP_ERR_UNSUPPORTED
+    rep = check_workload(mp, wl, WL.generate(wl), check_csr_tables=4)
+    _report("max capacity", rep)
+    assert rep["match_mode"] == mp.MP_MATCH_CSR and rep["heads"] == 8
 
 
 # ----------------------------------------------------------------------------------
