@@ -122,6 +122,28 @@ def test_near_tie_mask_flags_small_projections():
     assert O.near_ties(x2, W).all()
 
 
+def test_near_tie_band_is_relative_to_both_norms():
+    """A near tie is a projection below 1e-5 of |x - c| |w_j|, so whether a sign is a
+    near tie depends only on the angle between x - c and w_j: rescaling x - c or any
+    column of W leaves the mask unchanged. Columns are built at chosen cosines with
+    x - c: +-0.5e-5 (ties), +-2e-5 and 0.3 (not ties)."""
+    rng = np.random.default_rng(12)
+    d = 8
+    c = rng.normal(size=d)
+    xc = rng.normal(size=d)
+    xh = xc / np.linalg.norm(xc)
+    e = rng.normal(size=d)
+    e -= (e @ xh) * xh
+    e /= np.linalg.norm(e)
+    cosines = [0.5e-5, -0.5e-5, 2e-5, -2e-5, 0.3]
+    W = np.stack([cs * xh + math.sqrt(1 - cs * cs) * e for cs in cosines], axis=1)
+    want = np.array([[True, True, False, False, False]])
+    for sx in [1.0, 1e-3, 1e4]:
+        for cols in [np.ones(5), np.array([1e-3, 1e4, 7.0, 0.02, 1e3])]:
+            got = O.near_ties((c + sx * xc)[None, :], W * cols[None, :], center=c)
+            np.testing.assert_array_equal(got, want, err_msg=f"x scale {sx}, column scales {cols}")
+
+
 # ----------------------------------------------------------------------------------
 # a7 collision / inclusion probability
 # ----------------------------------------------------------------------------------
@@ -304,6 +326,27 @@ def test_translation_of_all_keys_changes_nothing():
     np.testing.assert_array_equal(a["S"], b["S"])
     assert len(a["S"]) > 0
     np.testing.assert_allclose(a["u"], b["u"], rtol=1e-10)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-9)
+
+
+def test_translation_invariance_covers_appended_tokens():
+    """Tokens appended after the build are hashed with the prefill's center, so a shift
+    of every key (prefill and appended) leaves all codes, the sampled set and the output
+    of a decode step past the prefill unchanged (MagicPIG §4.3 "Data pre-processing")."""
+    rng = np.random.default_rng(13)
+    d, n0, n, K, L, s, w = 16, 500, 560, 4, 20, 4, 32
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    shift = 5 * rng.normal(size=d)
+    ta = O.HeadTables(keys, W, K, L, s, n0, n_total=n)
+    tb = O.HeadTables(keys + shift, W, K, L, s, n0, n_total=n)
+    np.testing.assert_allclose(tb.center, ta.center + shift, rtol=1e-12)
+    np.testing.assert_array_equal(ta.codes, tb.codes)
+    a = O.decode_head(q, keys, vals, ta, n, w)
+    b = O.decode_head(q, keys + shift, vals, tb, n, w)
+    np.testing.assert_array_equal(a["S"], b["S"])
+    assert np.any(a["S"] >= n0)
     np.testing.assert_allclose(a["out"], b["out"], rtol=1e-9)
 
 
