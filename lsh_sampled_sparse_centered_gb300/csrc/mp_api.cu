@@ -204,10 +204,10 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;  // GB300
   if (cache[dev] == 0) {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
     cache[dev] = v;
   }
   return cache[dev];
@@ -226,9 +226,10 @@ static bool rows_on_tensor_cores(const Geometry& g, const TablesPtrs& t) {
          !use_simt_hash();
 }
 
-// Number of slices per query head for the attention: about 256 list entries per
+// Number of slices per query head for the attention: about 1024 list entries per
 // slice (estimated from the closed-form budget at p = 1/2), at most kSplitsMax. The
-// attention kernel is persistent, so the slices only need to be many and even.
+// attention kernel is persistent and takes slices from a work queue, so slices only
+// need to be many enough to spread the long lists over the SMs.
 static int choose_splits(const Geometry& g, int n) {
   const double x = std::ldexp(1.0, -g.K);
   double frac;
