@@ -568,7 +568,8 @@ def oracle_sample(wl, decode_steps: int = 4):
     job_s = t_build * U + t_dec * (total_q / nq)
     desc = (f"one KV head (layer 0, sequence 0, head 0): table build over {cap} tokens "
             f"({t_build:.2f} s) + {len(steps)} decode steps x {wl.group} query heads ({t_dec:.2f} s); "
-            f"job time scaled by {U} heads and {total_q} queries")
+            f"job time scaled by {U} heads and {total_q} queries; one process: numpy's BLAS "
+            f"matrix products may use all {cpu_cores()} cores, everything else runs on one thread")
     return total_q / job_s, t_build + t_dec, desc
 
 
