@@ -52,3 +52,44 @@ def test_isotropic_mix_fraction():
     k = WL.keys_block(wl, 0, 1, 0, 1, 20001)
     frac = ((k @ mu) < 1.0).double().mean().item()   # cone keys sit near 3 along mu
     assert 0.08 < frac < 0.13
+
+
+def _generate_block_by_block(wl):
+    """The tensors of generate() assembled from the one-block functions."""
+    cap, d = wl.capacity, wl.head_dim
+    keys = torch.zeros(wl.layers, wl.batch, wl.kv_heads, cap, d, dtype=wl.torch_dtype)
+    values = torch.zeros_like(keys)
+    queries = torch.zeros(wl.steps, wl.layers, wl.batch, wl.q_heads, d, dtype=wl.torch_dtype)
+    for l in range(wl.layers):
+        for b in range(wl.batch):
+            for h in range(wl.kv_heads):
+                keys[l, b, h] = WL.round_to(WL.keys_block(wl, l, b, h, 0, cap), wl.dtype)
+                values[l, b, h] = WL.round_to(WL.values_block(wl, l, b, h, 0, cap), wl.dtype)
+            for s in range(wl.steps):
+                queries[s, l, b] = WL.round_to(WL.query_block(wl, s, l, b), wl.dtype)
+    return keys, values, queries
+
+
+def test_generate_equals_the_block_functions():
+    """generate() draws all heads and steps of a sequence at once; every element must be
+    the one the single-block functions give."""
+    cases = [WL.WORKLOADS[0],
+             WL.Workload("mix", layers=2, batch=2, kv_heads=3, q_heads=6, head_dim=128, n_prefill=1037,
+                         steps=5, append=True, K=6, L=20, dtype="bf16", seed=17, iso_fraction=0.1,
+                         w_per_layer=True),
+             WL.WORKLOADS[1].replace(n_prefill=3000, steps=3)]
+    for wl in cases:
+        t = WL.generate(wl)
+        k, v, q = _generate_block_by_block(wl)
+        assert torch.equal(t["keys"], k), wl.name
+        assert torch.equal(t["values"], v), wl.name
+        assert torch.equal(t["queries"], q), wl.name
+
+
+def test_stream_draws_equal_single_stream_draws():
+    keys = [WL.stream_key(5, i) for i in range(4)]
+    g = WL.gaussian_streams(keys, 1000, offset=77)
+    u = WL.uniform_streams(keys, 333, offset=5)
+    for i, key in enumerate(keys):
+        assert torch.equal(g[i], WL.gaussian(key, 1000, offset=77))
+        assert torch.equal(u[i], WL.uniform(key, 333, offset=5))

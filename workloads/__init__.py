@@ -28,7 +28,7 @@ import torch
 __all__ = [
     "Workload", "WORKLOADS", "stream_key", "uniform", "gaussian",
     "head_mu", "keys_block", "values_block", "query_block", "projection",
-    "generate", "round_to",
+    "generate", "round_to", "uniform_streams", "gaussian_streams",
 ]
 
 _M32 = 0xFFFFFFFF
@@ -172,6 +172,30 @@ def gaussian(key: tuple[int, int], count: int, device="cpu", offset: int = 0) ->
     return torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
 
 
+def _bits_streams(keys: list[tuple[int, int]], counter: torch.Tensor) -> torch.Tensor:
+    """``_bits`` for several streams at once: [len(keys), len(counter)], row s equal to
+    ``_bits(keys[s], counter)`` element by element."""
+    a = torch.tensor([k[0] for k in keys], dtype=torch.int64, device=counter.device)[:, None]
+    b = torch.tensor([k[1] for k in keys], dtype=torch.int64, device=counter.device)[:, None]
+    return _fmix32(_fmix32((counter[None, :] + a) & _M32) ^ b)
+
+
+def uniform_streams(keys: list[tuple[int, int]], count: int, device="cpu", offset: int = 0) -> torch.Tensor:
+    """Row s equals ``uniform(keys[s], count, device, offset)``."""
+    ctr = torch.arange(offset, offset + count, dtype=torch.int64, device=device)
+    h = _bits_streams(keys, ctr)
+    return ((h >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
+
+
+def gaussian_streams(keys: list[tuple[int, int]], count: int, device="cpu", offset: int = 0) -> torch.Tensor:
+    """Row s equals ``gaussian(keys[s], count, device, offset)``: one set of kernel
+    launches for many streams instead of one per stream."""
+    ctr = torch.arange(offset, offset + count, dtype=torch.int64, device=device) * 2
+    u1 = ((_bits_streams(keys, ctr) >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
+    u2 = ((_bits_streams(keys, ctr + 1) >> 8).to(torch.float64) + 0.5) * (1.0 / 16777216.0)
+    return torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
+
+
 def round_to(x: torch.Tensor, dtype: str) -> torch.Tensor:
     return x.to(torch.bfloat16) if dtype == "bf16" else x.to(torch.float32)
 
@@ -247,14 +271,30 @@ def generate(wl: Workload, device="cpu", layers: Optional[list[int]] = None,
     keys = torch.zeros(shape, dtype=dt, device=device)
     values = torch.zeros(shape, dtype=dt, device=device) if with_values else None
     queries = torch.zeros(wl.steps, wl.layers, wl.batch, wl.q_heads, d, dtype=dt, device=device)
+    # the same values as keys_block / values_block / query_block, drawn for all KV heads
+    # (and all decode steps) of a sequence at once to keep the number of launches small
+    H = wl.kv_heads
+    q_head_kv = torch.arange(wl.q_heads, device=device) // wl.group
     for l in lay:
         for b in range(wl.batch):
-            for h in range(wl.kv_heads):
-                keys[l, b, h] = round_to(keys_block(wl, l, b, h, 0, cap, device), wl.dtype)
-                if with_values:
-                    values[l, b, h] = round_to(values_block(wl, l, b, h, 0, cap, device), wl.dtype)
-            for s in range(wl.steps):
-                queries[s, l, b] = round_to(query_block(wl, s, l, b, device), wl.dtype)
+            mus = torch.stack([head_mu(wl, l, b, h, device) for h in range(H)])
+            noise = gaussian_streams([stream_key(wl.seed, P_KEY, l, b, h) for h in range(H)], cap * d,
+                                     device).view(H, cap, d)
+            k = noise + 3.0 * mus[:, None, :]
+            if wl.iso_fraction > 0.0:
+                pick = uniform_streams([stream_key(wl.seed, P_MIX, l, b, h) for h in range(H)], cap, device)
+                k = torch.where((pick < wl.iso_fraction)[:, :, None], noise, k)
+            if cap > 0:
+                k[:, 0] = -6.0 * mus
+            keys[l, b] = round_to(k, wl.dtype)
+            del noise, k
+            if with_values:
+                values[l, b] = round_to(gaussian_streams([stream_key(wl.seed, P_VALUE, l, b, h) for h in range(H)],
+                                                         cap * d, device).view(H, cap, d), wl.dtype)
+            if wl.steps > 0:
+                qn = gaussian_streams([stream_key(wl.seed, P_QUERY, s, l, b) for s in range(wl.steps)],
+                                      wl.q_heads * d, device).view(wl.steps, wl.q_heads, d)
+                queries[:, l, b] = round_to(qn - 2.0 * mus[q_head_kv][None], wl.dtype)
     nw = wl.layers if wl.w_per_layer else 1
     W = torch.stack([projection(wl, l, device) for l in range(nw)])
     return {"keys": keys, "values": values, "W": W, "queries": queries}
