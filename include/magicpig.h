@@ -183,7 +183,10 @@ MP_API int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_pre
  * L tables (one decode-step append). The caller has already written
  * keys[..][pos][:]. Uses the center fixed at build time. Tokens appended this way
  * are matched by comparing stored codes once they leave the window.
- * n_prefill <= pos < capacity, else MP_ERR_CAPACITY. */
+ * 0 <= pos < capacity, else MP_ERR_CAPACITY. pos is meant to be the next token,
+ * pos >= n_prefill; the host cannot check that bound (n_prefill lives in the device
+ * header). An append at pos < n_prefill rewrites that token's stored code (and its
+ * bit-planes in scan mode) but not its place in the CSR buckets built at build time. */
 MP_API int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream);
 
 /* One decode step for every query head (Algorithm 1 with the exact sink/window
