@@ -169,7 +169,8 @@ MP_API int mp_decode_layout_get(const mp_config* cfg, mp_decode_layout* out);
  * (layer, sequence, KV head): center with the mean of keys [n_sink, n_prefill)
  * (§4.3 "Data pre-processing"), SimHash every prefill key into L K-bit codes with
  * the projections W (§2.2, §4.3, Algorithm 1 'Encode'; on bf16 keys the projection
- * runs on tensor cores and W must be bf16-representable, else MP_STATUS_W_NOT_BF16),
+ * runs on tensor cores, through W's exact three-term bf16 split when W is not
+ * bf16-representable, which the informational MP_STATUS_W_NOT_BF16 bit reports),
  * and bucket the ids of tokens [n_sink, n_prefill) per (head, table, code) —
  * the hash tables HT of Algorithm 1.
  *   keys    : device, layout above; rows [0, n_prefill) are read.
