@@ -18,7 +18,7 @@ import math
 
 import numpy as np
 
-NEAR_TIE_REL = 1e-5   # a projection with |y| < 1e-5 * ||x|| * ||w_j|| is a near tie
+NEAR_TIE_REL = 1e-5   # a projection with |y| <= 1e-5 * ||x|| * ||w_j|| is a near tie
 THRESHOLD = 2         # [MagicPIG] §4.3 "Hash function selection": at least two tables
 
 
@@ -59,15 +59,20 @@ def projections(x, W, center=None) -> np.ndarray:
 
 
 def near_ties(x, W, center=None) -> np.ndarray:
-    """Mask [n, K·L] of projections with |y| < 1e-5 * ||x - center|| * ||W[:, j]||.
+    """Mask [n, K·L] of projections with |y| <= 1e-5 * ||x - center|| * ||W[:, j]||.
     These sign decisions are too close to zero to be reproduced bit-exactly by
-    fp32 arithmetic, so comparisons exclude them (and count them)."""
+    fp32 arithmetic, so comparisons exclude them (and count them).
+
+    READING: the band is closed, so an exact zero projection is always a near tie,
+    also when x equals the center (both sides zero). SimHash keeps the sign of the
+    projection ([MagicPIG] §2.2), which a zero projection does not have; its bit is a
+    convention of each implementation and is not compared."""
     x = _f64(x)
     if center is not None:
         x = x - _f64(center)[None, :]
     y = x @ _f64(W)
     bound = NEAR_TIE_REL * np.linalg.norm(x, axis=1)[:, None] * np.linalg.norm(_f64(W), axis=0)[None, :]
-    return np.abs(y) < bound
+    return np.abs(y) <= bound
 
 
 def simhash_codes(x, W, K: int, L: int, center=None) -> np.ndarray:

@@ -141,6 +141,11 @@ MUTANTS = {
     "near-tie band without the column norm": {
         "near_ties": lambda x, W, center=None: np.abs(M.projections(x, W, center)) < M.NEAR_TIE_REL * np.linalg.norm(
             np.asarray(x, float) - (0 if center is None else np.asarray(center, float)[None, :]), axis=1)[:, None]},
+    "near-tie band open (exact zeros compared)": {
+        "near_ties": lambda x, W, center=None: (lambda x0: np.abs(x0 @ np.asarray(W, float)) < M.NEAR_TIE_REL
+                                                * np.linalg.norm(x0, axis=1)[:, None]
+                                                * np.linalg.norm(np.asarray(W, float), axis=0)[None, :])(
+            np.asarray(x, float) - (0 if center is None else np.asarray(center, float)[None, :]))},
     "query hashed centered": {"decode_head": _decode_head_centered_query},
     "appended tokens hashed uncentered": {"HeadTables": _TablesAppendedUncentered},
     # a6 match and region

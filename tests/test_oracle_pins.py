@@ -122,6 +122,17 @@ def test_near_tie_mask_flags_small_projections():
     assert O.near_ties(x2, W).all()
 
 
+def test_zero_projections_are_near_ties():
+    """SimHash keeps the sign of a projection ([MagicPIG] §2.2); a projection that is
+    exactly zero has none, so it is a near tie and its bit is never compared: a key
+    equal to the center, a zero query, and a column orthogonal to the key."""
+    W = np.array([[1.0, 0.0, 2.0], [0.0, 1.0, -1.0]])
+    c = np.array([0.5, -0.25])
+    assert O.near_ties(c[None, :], W, center=c).all()
+    assert O.near_ties(np.zeros((1, 2)), W).all()
+    np.testing.assert_array_equal(O.near_ties(np.array([[1.0, 2.0]]), W), [[False, False, True]])
+
+
 def test_near_tie_band_is_relative_to_both_norms():
     """A near tie is a projection below 1e-5 of |x - c| |w_j|, so whether a sign is a
     near tie depends only on the angle between x - c and w_j: rescaling x - c or any
