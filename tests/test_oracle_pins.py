@@ -324,6 +324,38 @@ def test_short_sequence_is_all_static_and_exact():
     np.testing.assert_allclose(r["out"], softmax(keys @ q / math.sqrt(d)) @ vals, rtol=1e-12)
 
 
+def test_constant_keys_reduce_to_a_weighted_mean():
+    """Degenerate head: every key equals the center, so every projection is zero (code 0
+    in every table, all near ties), cos(q, k - c) is taken as 0 (p = 1/2) and all logits
+    are equal. The sampled set is the whole region or nothing, depending on whether the
+    query's code is 0 in at least two tables, and the output is the mean of the values
+    with weight 1/u on the sampled tokens and 1 on the static ones."""
+    rng = np.random.default_rng(21)
+    d, n, K, L, s, w = 8, 120, 2, 6, 4, 16
+    a = np.round(16 * rng.normal(size=d)) / 16   # few mantissa bits: the mean is exactly a
+    keys = np.tile(a, (n, 1))
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    t = O.HeadTables(keys, W, K, L, s, n)
+    assert np.all(t.codes == 0) and t.ties.all()
+    u_half = O.inclusion_probability(np.array([0.5]), K, L)[0]
+    seen = set()
+    for _ in range(40):
+        q = rng.normal(size=d)
+        r = O.decode_head(q, keys, vals, t, n, w)
+        region = np.arange(s, n - w)
+        zero_tables = int(np.sum(r["q_code"] == 0))
+        S = region if zero_tables >= 2 else region[:0]
+        np.testing.assert_array_equal(r["S"], S)
+        np.testing.assert_allclose(r["p"], 0.5)
+        wts = np.ones(n)
+        wts[S] = 1.0 / u_half
+        wts[np.setdiff1d(region, S)] = 0.0
+        np.testing.assert_allclose(r["out"], wts @ vals / wts.sum(), rtol=1e-12)
+        seen.add(len(S) > 0)
+    assert seen == {True, False}
+
+
 def test_translation_of_all_keys_changes_nothing():
     """Softmax is translation invariant and keys are centered (MagicPIG §4.3)."""
     rng = np.random.default_rng(9)
