@@ -410,3 +410,57 @@ def test_centering_off_hashes_raw_keys_and_is_not_translation_invariant():
     np.testing.assert_array_equal(on_a.codes, on_b.codes)
     off_b = O.HeadTables(keys + shift, W, K, L, s, n0, centering=False)
     assert np.any(off_b.codes != off.codes)
+
+
+# ----------------------------------------------------------------------------------
+# invariances of the whole step
+# ----------------------------------------------------------------------------------
+
+def test_tables_are_exchangeable_and_hyperplanes_scale_free():
+    """Relabelling the L tables (moving whole K-column blocks of W) or scaling any
+    hyperplane by a positive factor changes no sign, so S, u and the output stay the
+    same (SimHash depends on the hyperplanes' directions only, MagicPIG §2.2)."""
+    rng = np.random.default_rng(23)
+    d, n, K, L, s, w = 12, 400, 3, 9, 4, 16
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    base = O.decode_head(q, keys, vals, O.HeadTables(keys, W, K, L, s, n), n, w)
+    assert len(base["S"]) > 0
+    perm = rng.permutation(L)
+    Wp = W.reshape(d, L, K)[:, perm, :].reshape(d, K * L)
+    Ws = W * rng.uniform(0.01, 100.0, size=K * L)[None, :]
+    for W2 in (Wp, Ws):
+        r = O.decode_head(q, keys, vals, O.HeadTables(keys, W2, K, L, s, n), n, w)
+        np.testing.assert_array_equal(r["S"], base["S"])
+        np.testing.assert_allclose(r["u"], base["u"], rtol=1e-12)
+        np.testing.assert_allclose(r["out"], base["out"], rtol=1e-12)
+
+
+def test_decode_reads_only_the_visible_tokens():
+    """A decode step over n tokens does not depend on keys or values at positions >= n."""
+    rng = np.random.default_rng(29)
+    d, n0, n, K, L, s, w = 12, 300, 340, 3, 10, 4, 16
+    keys, q = _cone(rng, d, n + 20)
+    vals = rng.normal(size=(n + 20, d))
+    W = rng.normal(size=(d, K * L))
+    t = O.HeadTables(keys, W, K, L, s, n0, n_total=n + 20)
+    a = O.decode_head(q, keys, vals, t, n, w)
+    keys2, vals2 = keys.copy(), vals.copy()
+    keys2[n:] = 100.0 * rng.normal(size=(20, d))
+    vals2[n:] = 100.0 * rng.normal(size=(20, d))
+    t2 = O.HeadTables(keys2, W, K, L, s, n0, n_total=n + 20)
+    b = O.decode_head(q, keys2, vals2, t2, n, w)
+    np.testing.assert_array_equal(a["S"], b["S"])
+    np.testing.assert_array_equal(a["out"], b["out"])
+
+
+def test_inclusion_probability_orders_with_K_L_and_T():
+    """More tables raise u, more bits per table and a higher threshold lower it
+    (P[Bin(L, p^K) >= T] is increasing in L and p, decreasing in K and T)."""
+    p = np.linspace(0.05, 0.95, 19)
+    u = lambda K, L, T: O.inclusion_probability(p, K, L, threshold=T)  # noqa: E731
+    assert np.all(u(4, 20, 2) < u(4, 21, 2))
+    assert np.all(u(5, 20, 2) < u(4, 20, 2))
+    assert np.all(u(4, 20, 3) < u(4, 20, 2))
+    assert np.all(np.diff(u(6, 50, 3)) > 0)
