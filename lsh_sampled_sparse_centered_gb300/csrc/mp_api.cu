@@ -1,5 +1,6 @@
 // Host side of the C ABI: validation, buffer layouts and the launch sequence of
 // each call. No device memory is allocated here; every buffer is the caller's.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -202,15 +203,16 @@ static bool injected(const char* what) {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  // per-device cache; callers on several host threads may fill it concurrently
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;  // GB300
-  if (cache[dev] == 0) {
-    int v = 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
-    cache[dev] = v;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 // Hash path for bf16 keys, queries and appends: tensor cores unless MP_HASH_PATH=simt.
