@@ -464,3 +464,67 @@ def test_inclusion_probability_orders_with_K_L_and_T():
     assert np.all(u(5, 20, 2) < u(4, 20, 2))
     assert np.all(u(4, 20, 3) < u(4, 20, 2))
     assert np.all(np.diff(u(6, 50, 3)) > 0)
+
+
+# ----------------------------------------------------------------------------------
+# brute force on tiny inputs: the step written with loops and the math module
+# ----------------------------------------------------------------------------------
+
+def _brute_force_step(q, keys, vals, W, K, L, s, w, n0, n, T=2):
+    """One decode step from the definitions, element by element, no numpy: the mean
+    key over [s, n0); bit b of table t = [<x - c, W[:, tK + b]> > 0]; sampled iff
+    >= T tables agree with the query; weights e^{q.k/sqrt d} / u on S, e^{q.k/sqrt d}
+    on the sinks and the window; u = sum_{j >= T} C(L, j) x^j (1 - x)^(L - j)."""
+    d = len(q)
+    c = [sum(keys[i][j] for i in range(s, n0)) / (n0 - s) for j in range(d)]
+
+    def code(x, center):
+        out = []
+        for t in range(L):
+            v = 0
+            for b in range(K):
+                y = sum((x[j] - center[j]) * W[j][t * K + b] for j in range(d))
+                v |= (1 if y > 0 else 0) << b
+            out.append(v)
+        return out
+
+    qc = code(q, [0.0] * d)
+    lo, hi = min(s, n), max(min(s, n), n - w)
+    num, den = [0.0] * d, 0.0
+    M = max(sum(q[j] * keys[i][j] for j in range(d)) / math.sqrt(d) for i in range(n))
+    S = []
+    for i in range(n):
+        z = sum(q[j] * keys[i][j] for j in range(d)) / math.sqrt(d)
+        wt = math.exp(z - M)
+        if lo <= i < hi:
+            kc = code(keys[i], c)
+            if sum(1 for t in range(L) if kc[t] == qc[t]) < T:
+                continue
+            S.append(i)
+            kd = [keys[i][j] - c[j] for j in range(d)]
+            nq = math.sqrt(sum(v * v for v in q))
+            nk = math.sqrt(sum(v * v for v in kd))
+            cs = sum(q[j] * kd[j] for j in range(d)) / (nq * nk) if nq * nk > 0 else 0.0
+            p = 1.0 - math.acos(max(-1.0, min(1.0, cs))) / math.pi
+            x = p ** K
+            u = sum(math.comb(L, j) * x ** j * (1 - x) ** (L - j) for j in range(T, L + 1))
+            wt /= u
+        den += wt
+        for j in range(d):
+            num[j] += wt * vals[i][j]
+    return S, [v / den for v in num]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_whole_step_equals_brute_force_on_tiny_inputs(seed):
+    rng = np.random.default_rng(100 + seed)
+    d, n0, n, K, L, s, w = 5, 37, 41, 2, 4, 2, 5
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    t = O.HeadTables(keys, W, K, L, s, n0, n_total=n)
+    r = O.decode_head(q, keys, vals, t, n, w)
+    S, out = _brute_force_step(q.tolist(), keys.tolist(), vals.tolist(), W.tolist(), K, L, s, w, n0, n)
+    assert len(S) > 0
+    np.testing.assert_array_equal(r["S"], S)
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12)
