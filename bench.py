@@ -16,7 +16,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -541,8 +540,6 @@ def oracle_sample(wl, decode_steps: int = 4):
     """Time the fp64 oracle on one KV head of the workload: its table build (all
     tokens hashed) and `decode_steps` decode steps for each of its query heads; scale
     to the whole job by unit counts. Returns (queries/s, seconds spent, description)."""
-    import numpy as np
-    import torch
 
     import oracle as O
     import workloads as WL

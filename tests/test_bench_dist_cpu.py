@@ -4,7 +4,6 @@ Replicas share nothing on the data path, so these are the only cross-rank steps.
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as tmp
 
 
