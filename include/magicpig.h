@@ -52,7 +52,8 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 2 /* 2: mp_config.no_centering, mp_tables_layout.negbeta_f32, three-term W */
+#define MP_ABI_VERSION 3 /* 2: mp_config.no_centering, mp_tables_layout.negbeta_f32, three-term W;
+                            3: mp_config.center_query */
 
 /* return codes */
 #define MP_OK 0
@@ -99,7 +100,11 @@ typedef struct mp_config {
   int32_t no_centering; /* 0 (default): keys are centered by their prefill mean before hashing
                            (pages §4.3 "Data pre-processing"); 1: hashed uncentered, c = 0 (the
                            pages' centering ablation) */
-  int32_t reserved[3]; /* must be zero */
+  int32_t center_query; /* 0 (default): the query is hashed as it is, p = 1 - theta(q, k - c)/pi
+                           (the pages center the keys only, §4.3); 1: the query is hashed after
+                           subtracting its KV head's center and p = 1 - theta(q - c, k - c)/pi.
+                           Not built on the CUDA path yet: 1 gives MP_ERR_UNSUPPORTED */
+  int32_t reserved[2]; /* must be zero */
 } mp_config;
 
 /* Byte offsets (from the start of the tables buffer) of the arrays the library keeps

@@ -45,8 +45,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 class mp_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "layers", "batch", "kv_heads", "q_heads", "head_dim", "K", "L", "n_sink", "window",
-        "capacity", "dtype", "w_per_layer", "match_mode", "threshold", "no_centering")] + [
-        ("reserved", ctypes.c_int32 * 3)]
+        "capacity", "dtype", "w_per_layer", "match_mode", "threshold", "no_centering", "center_query")] + [
+        ("reserved", ctypes.c_int32 * 2)]
 
 
 class mp_tables_layout(ctypes.Structure):
@@ -132,11 +132,13 @@ def _check(fn: str, rc: int) -> int:
 
 def make_config(*, layers: int, batch: int, kv_heads: int, q_heads: int, head_dim: int, K: int, L: int,
                 n_sink: int, window: int, capacity: int, dtype: Union[int, str], w_per_layer: bool = False,
-                match_mode: int = MP_MATCH_AUTO, threshold: int = 2, centering: bool = True) -> mp_config:
+                match_mode: int = MP_MATCH_AUTO, threshold: int = 2, centering: bool = True,
+                center_query: bool = False) -> mp_config:
     if isinstance(dtype, str):
         dtype = MP_DTYPE_BF16 if dtype == "bf16" else MP_DTYPE_F32
     return mp_config(layers, batch, kv_heads, q_heads, head_dim, K, L, n_sink, window, capacity, int(dtype),
-                     int(bool(w_per_layer)), match_mode, threshold, 0 if centering else 1)
+                     int(bool(w_per_layer)), match_mode, threshold, 0 if centering else 1,
+                     int(bool(center_query)))
 
 
 def mp_abi_version() -> int:

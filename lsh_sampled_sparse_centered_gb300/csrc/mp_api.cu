@@ -35,9 +35,11 @@ static int check_config(const mp_config* c) {
   if (c->match_mode != MP_MATCH_AUTO && c->match_mode != MP_MATCH_CSR && c->match_mode != MP_MATCH_SCAN)
     return MP_ERR_INVALID_ARG;
   if (c->threshold < 1 || c->threshold > c->L) return MP_ERR_INVALID_ARG;
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 2; ++i)
     if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
   if (c->no_centering != 0 && c->no_centering != 1) return MP_ERR_INVALID_ARG;
+  if (c->center_query != 0 && c->center_query != 1) return MP_ERR_INVALID_ARG;
+  if (c->center_query) return MP_ERR_UNSUPPORTED;  // centered-query hashing: oracle only so far
   if (c->head_dim != 64 && c->head_dim != 128) return MP_ERR_UNSUPPORTED;
   if (c->K > kMaxK || c->L > kMaxL || c->capacity > kMaxCapacity) return MP_ERR_UNSUPPORTED;
   // thresholds above 2: at most 7 (3-bit counters in the scan), L <= 255 (byte counters

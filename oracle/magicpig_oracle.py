@@ -283,24 +283,29 @@ class HeadTables:
 
 
 def decode_head(q, keys, values, tables: HeadTables, n: int, window: int,
-                threshold: int = THRESHOLD, key_codes=None, q_code=None) -> dict:
+                threshold: int = THRESHOLD, key_codes=None, q_code=None, center_query: bool = False) -> dict:
     """One decode step for one query head ([MagicPIG] Algorithm 1 with the on-device
     cache of §4.4): encode q, query the tables, weight the sampled keys by -log u,
     attend exactly over sinks and window.
 
-    READING: the query is hashed uncentered (only keys are centered in §4.3).
-    `key_codes` / `q_code` may be given to run the later steps on codes computed
-    elsewhere (stage-wise checks). Returns a dict with the intermediate results.
+    READING: the query is hashed uncentered (only keys are centered in §4.3), and the
+    collision probability is that of q with the centered key. With center_query the
+    other reading is taken: q - c is hashed and p is the collision probability of
+    q - c with k - c, the pair of vectors whose signs are compared. The logits use
+    the raw q and k in both readings. `key_codes` / `q_code` may be given to run the
+    later steps on codes computed elsewhere (stage-wise checks). Returns a dict with
+    the intermediate results.
     """
     q = _f64(q)
     K, L, s = tables.K, tables.L, tables.n_sink
-    qc = simhash_codes(q[None, :], tables.W, K, L)[0] if q_code is None else np.asarray(q_code)
+    qh = q - tables.center if center_query else q   # the vector that is hashed
+    qc = simhash_codes(qh[None, :], tables.W, K, L)[0] if q_code is None else np.asarray(q_code)
     kc = tables.codes[:n] if key_codes is None else np.asarray(key_codes)[:n]
     counts = match_counts(kc, qc)
     S = sampled_set(counts, n, s, window, threshold)
     T = exact_tokens(n, s, window)
     k64 = _f64(keys)[:n]
-    p = collision_probability(q, k64[S] - tables.center[None, :])
+    p = collision_probability(qh, k64[S] - tables.center[None, :])
     u = inclusion_probability(p, K, L, threshold)
     o = snis_attention(q, k64, _f64(values)[:n], S, u, T)
     return {"q_code": qc, "counts": counts, "S": S, "T": T, "p": p, "u": u, "out": o}

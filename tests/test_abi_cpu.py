@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(mp):
     for n in names:
         assert getattr(lib, n) is not None
     assert set(mp.EXPORTED) <= set(names)
-    assert mp.mp_abi_version() == 2
+    assert mp.mp_abi_version() == 3
 
 
 def _cfg(mp, **kw):
@@ -58,11 +58,16 @@ def test_config_validation(mp):
     for u in unsup:
         assert mp.mp_config_check(_cfg(mp, **u)) == mp.MP_ERR_UNSUPPORTED, u
     c = _cfg(mp)
-    c.reserved[2] = 1
+    c.reserved[1] = 1
     assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
     assert mp.mp_config_check(_cfg(mp, centering=False)) == mp.MP_OK
     c = _cfg(mp)
     c.no_centering = 2
+    assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
+    # the centered-query reading is not built on the CUDA path yet
+    assert mp.mp_config_check(_cfg(mp, center_query=True)) == mp.MP_ERR_UNSUPPORTED
+    c = _cfg(mp)
+    c.center_query = 2
     assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
 
 

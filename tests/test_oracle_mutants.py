@@ -100,19 +100,29 @@ def _u_closed_form_as_printed(p, K, L, threshold=M.THRESHOLD):
 
 
 def _decode_head_p_from_raw_keys(q, keys, values, tables, n, window, threshold=M.THRESHOLD, key_codes=None,
-                                 q_code=None):
-    r = ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, q_code)
+                                 q_code=None, center_query=False):
+    r = ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, q_code, center_query)
     k64 = np.asarray(keys, float)[:n]
-    p = M.collision_probability(q, k64[r["S"]])
+    qh = np.asarray(q, float) - (tables.center if center_query else 0.0)
+    p = M.collision_probability(qh, k64[r["S"]])
     u = M.inclusion_probability(p, tables.K, tables.L, threshold)
     out = M.snis_attention(q, k64, np.asarray(values, float)[:n], r["S"], u, r["T"])
     return {**r, "p": p, "u": u, "out": out}
 
 
 def _decode_head_centered_query(q, keys, values, tables, n, window, threshold=M.THRESHOLD, key_codes=None,
-                                q_code=None):
+                                q_code=None, center_query=False):
     qc = M.simhash_codes(np.asarray(q, float)[None, :], tables.W, tables.K, tables.L, tables.center)[0]
-    return ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, qc)
+    return ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, qc, center_query)
+
+
+def _decode_head_centered_hash_raw_p(q, keys, values, tables, n, window, threshold=M.THRESHOLD, key_codes=None,
+                                     q_code=None, center_query=False):
+    """Centered-query reading with p taken from the raw query."""
+    if not center_query:
+        return ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, q_code)
+    qc = M.simhash_codes(np.asarray(q, float)[None, :], tables.W, tables.K, tables.L, tables.center)[0]
+    return ORIG["decode_head"](q, keys, values, tables, n, window, threshold, key_codes, qc, False)
 
 
 class _TablesAppendedUncentered(ORIG["HeadTables"]):
@@ -147,6 +157,7 @@ MUTANTS = {
                                                 * np.linalg.norm(np.asarray(W, float), axis=0)[None, :])(
             np.asarray(x, float) - (0 if center is None else np.asarray(center, float)[None, :]))},
     "query hashed centered": {"decode_head": _decode_head_centered_query},
+    "centered query with p from the raw query": {"decode_head": _decode_head_centered_hash_raw_p},
     "appended tokens hashed uncentered": {"HeadTables": _TablesAppendedUncentered},
     # a6 match and region
     "query codes shifted by one table": {

@@ -528,3 +528,80 @@ def test_whole_step_equals_brute_force_on_tiny_inputs(seed):
     assert len(S) > 0
     np.testing.assert_array_equal(r["S"], S)
     np.testing.assert_allclose(r["out"], out, rtol=1e-12)
+
+
+
+# ----------------------------------------------------------------------------------
+# the centered-query reading (query hashed as q - c)
+# ----------------------------------------------------------------------------------
+
+def test_centered_query_sampling_rule_matches_its_inclusion_probability():
+    """With q - c hashed, each key is sampled with probability u_i computed from
+    p = 1 - theta(q - c, k - c)/pi, the pair of vectors whose signs are compared: the
+    frequency of every key over independent hash draws agrees with that u_i (and, for
+    the keys where the readings differ most, not with the u of the uncentered query)."""
+    rng = np.random.default_rng(31)
+    d, n, K, L, s, w = 10, 300, 3, 10, 4, 16
+    keys, q = _cone(rng, d, n)
+    lo, hi = O.lsh_region(n, s, w)
+    draws = 600
+    hits = np.zeros(hi - lo)
+    center = None
+    for _ in range(draws):
+        W = rng.normal(size=(d, K * L))
+        t = O.HeadTables(keys, W, K, L, s, n)
+        center = t.center
+        r = O.decode_head(q, keys, keys, t, n, w, center_query=True)
+        hits[r["S"] - lo] += 1
+    freq = hits / draws
+    u_cq = O.inclusion_probability(O.collision_probability(q - center, keys[lo:hi] - center), K, L)
+    u_raw = O.inclusion_probability(O.collision_probability(q, keys[lo:hi] - center), K, L)
+    se = np.sqrt(np.maximum(u_cq * (1 - u_cq), 1e-4) / draws)
+    assert np.all(np.abs(freq - u_cq) < 5 * se), np.max(np.abs(freq - u_cq) / se)
+    far = np.argsort(-np.abs(u_cq - u_raw))[:5]
+    assert np.all(np.abs(freq[far] - u_raw[far]) > 5 * se[far])
+
+
+def test_centered_query_sets_are_invariant_to_a_common_shift():
+    """Shifting every key and the query by one vector leaves q - c and k - c, hence the
+    codes, the sampled set and u, unchanged in the centered-query reading (but not the
+    logits, which use the raw vectors)."""
+    rng = np.random.default_rng(37)
+    d, n, K, L, s, w = 16, 600, 4, 20, 4, 32
+    keys, q = _cone(rng, d, n)
+    vals = rng.normal(size=(n, d))
+    W = rng.normal(size=(d, K * L))
+    shift = 5 * rng.normal(size=d)
+    a = O.decode_head(q, keys, vals, O.HeadTables(keys, W, K, L, s, n), n, w, center_query=True)
+    b = O.decode_head(q + shift, keys + shift, vals, O.HeadTables(keys + shift, W, K, L, s, n), n, w,
+                      center_query=True)
+    np.testing.assert_array_equal(a["q_code"], b["q_code"])
+    np.testing.assert_array_equal(a["S"], b["S"])
+    assert len(a["S"]) > 0
+    np.testing.assert_allclose(a["u"], b["u"], rtol=1e-10)
+
+
+def test_each_key_is_sampled_with_its_inclusion_probability():
+    """Per key, not only in the sum: over independent hash draws every key of the LSH
+    region is sampled with frequency u_i (the uncentered query's p with the centered
+    key), and the keys where the two query readings differ most reject the other one."""
+    rng = np.random.default_rng(41)
+    d, n, K, L, s, w = 10, 300, 3, 10, 4, 16
+    keys, q = _cone(rng, d, n)
+    lo, hi = O.lsh_region(n, s, w)
+    draws = 600
+    hits = np.zeros(hi - lo)
+    center = None
+    for _ in range(draws):
+        W = rng.normal(size=(d, K * L))
+        t = O.HeadTables(keys, W, K, L, s, n)
+        center = t.center
+        r = O.decode_head(q, keys, keys, t, n, w)
+        hits[r["S"] - lo] += 1
+    freq = hits / draws
+    u = O.inclusion_probability(O.collision_probability(q, keys[lo:hi] - center), K, L)
+    u_other = O.inclusion_probability(O.collision_probability(q - center, keys[lo:hi] - center), K, L)
+    se = np.sqrt(np.maximum(u * (1 - u), 1e-4) / draws)
+    assert np.all(np.abs(freq - u) < 5 * se), np.max(np.abs(freq - u) / se)
+    far = np.argsort(-np.abs(u - u_other))[:5]
+    assert np.all(np.abs(freq[far] - u_other[far]) > 5 * se[far])
