@@ -55,3 +55,20 @@ def test_reference_arm_line_on_tiny_workload():
     line = bench.run_reference(args, rank=0, world=1)
     assert line["impl"] == "reference" and line["unit"] == "queries/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_command_line_prints_one_json_line():
+    """The command the reference arm is launched with, end to end on the CPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "0",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=300, check=True)
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 1 and line["n_gpus"] == 1
