@@ -102,8 +102,9 @@ typedef struct mp_config {
                            pages' centering ablation) */
   int32_t center_query; /* 0 (default): the query is hashed as it is, p = 1 - theta(q, k - c)/pi
                            (the pages center the keys only, §4.3); 1: the query is hashed after
-                           subtracting its KV head's center and p = 1 - theta(q - c, k - c)/pi.
-                           Not built on the CUDA path yet: 1 gives MP_ERR_UNSUPPORTED */
+                           subtracting its KV head's center and p = 1 - theta(q - c, k - c)/pi,
+                           the probability that the two vectors whose signs are compared share a
+                           table's code (§2.2 SimHash). The logits use the raw q and k either way */
   int32_t reserved[2]; /* must be zero */
 } mp_config;
 
@@ -196,7 +197,7 @@ MP_API int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_pre
 MP_API int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream);
 
 /* One decode step for every query head (Algorithm 1 with the exact sink/window
- * cache of §4.4): hash q (uncentered), collect S = {i in [n_sink, n - window) :
+ * cache of §4.4): hash q (or q - c with config.center_query), collect S = {i in [n_sink, n - window) :
  * code equal in >= threshold tables}, and write
  *   out = softmax([q·k_S/√d − log u_S, q·k_T/√d]) [V_S; V_T]
  * with T the sinks [0, n_sink) and the window [n - window, n), u = 1 on T.
@@ -224,7 +225,10 @@ MP_API int mp_decode_attention(const mp_config* cfg, void* tables, const void* k
  * exits. Calls whose mp_decode_layout_get(cfg).total_bytes exceeds that size are
  * rejected with MP_ERR_SCRATCH before anything is enqueued. The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture. Allocates nothing
+ * current) and keeps it for the life of the process; make that first call before any
+ * stream capture. The kept address assumes the device's primary context lives as long
+ * as the process: after cudaDeviceReset the module is loaded again and the array may
+ * move, so a process that resets a device must not call this entry point afterwards. Allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine). All calls share the array
  * and it keeps the last call's contents; the counters that must start at zero are
  * reset on the device by every call. Calls whose kernels overlap on the GPU race on

@@ -39,7 +39,6 @@ static int check_config(const mp_config* c) {
     if (c->reserved[i] != 0) return MP_ERR_INVALID_ARG;
   if (c->no_centering != 0 && c->no_centering != 1) return MP_ERR_INVALID_ARG;
   if (c->center_query != 0 && c->center_query != 1) return MP_ERR_INVALID_ARG;
-  if (c->center_query) return MP_ERR_UNSUPPORTED;  // centered-query hashing: oracle only so far
   if (c->head_dim != 64 && c->head_dim != 128) return MP_ERR_UNSUPPORTED;
   if (c->K > kMaxK || c->L > kMaxL || c->capacity > kMaxCapacity) return MP_ERR_UNSUPPORTED;
   // thresholds above 2: at most 7 (3-bit counters in the scan), L <= 255 (byte counters
@@ -78,6 +77,7 @@ static Geometry geometry(const mp_config* c) {
   g.w_per_layer = c->w_per_layer;
   g.threshold = c->threshold;
   g.no_center = c->no_centering;
+  g.center_query = c->center_query;
   g.group = c->q_heads / c->kv_heads;
   g.units = c->layers * c->batch * c->kv_heads;
   g.queries = c->layers * c->batch * c->q_heads;
@@ -385,6 +385,7 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
     a.center = t.center;
     a.c_gs = 1;
     a.c_rs = 0;
+    a.c_div = 1;
     a.wt = t.wt32;
     a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
     a.groups_per_w = g.batch * g.kvh;
@@ -427,6 +428,7 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   a.center = t.center;
   a.c_gs = g.batch * g.kvh;
   a.c_rs = 1;
+  a.c_div = 1;
   a.wt = t.wt32;
   a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
@@ -451,11 +453,13 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
     h.groups_per_w = 1;
     h.wt16 = t.wt16;
     h.negbeta = t.negbeta;
+    h.nb_div = 1;
     h.out = t.codes + pos;
     h.out_gs = a.out_gs;
     h.out_rs = a.out_rs;
     h.out_ts = a.out_ts;
     h.hdr = t.hdr;
+    h.mark = 1;
     h.mark_pos = pos;
     ProfScope ps(st, K_HASH_APPEND);
     if (launch_hash_rows_tc(g, h, st) != cudaSuccess) return MP_ERR_CUDA;
@@ -493,7 +497,9 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   const DecodePtrs dp = decode_ptrs(g, scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  // 1. query codes (Algorithm 1 'Encode'); the query is not centered
+  // 1. query codes (Algorithm 1 'Encode'): the query as it is, or (center_query) the
+  // query minus the center of its KV head, query head j of a sequence using KV head
+  // j / group
   HashRowsArgs a;
   std::memset(&a, 0, sizeof(a));
   a.src = q;
@@ -502,7 +508,10 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   a.rows = g.batch * g.qh;
   a.groups = g.layers;
   a.row0 = 0;
-  a.center = nullptr;
+  a.center = g.center_query ? t.center : nullptr;
+  a.c_gs = int64_t(g.batch) * g.kvh;
+  a.c_rs = 1;
+  a.c_div = g.group;
   a.wt = t.wt32;
   a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
@@ -522,7 +531,8 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
     h.groups = g.layers;
     h.groups_per_w = 1;
     h.wt16 = t.wt16;
-    h.negbeta = nullptr;
+    h.negbeta = g.center_query ? t.negbeta : nullptr;
+    h.nb_div = g.group;
     h.out = dp.qcodes;
     h.out_gs = a.out_gs;
     h.out_rs = a.out_rs;

@@ -7,6 +7,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "mp_compact.cuh"
 #include "mp_internal.h"
@@ -283,8 +284,14 @@ __device__ __forceinline__ int row_lane(int sub, int u) {
   return sub * LPR + (u >> 2) * (LPR / 2) + ((u >> 1) & 1) * (LPR / 4) + (u & 1) * (LPR / 8);
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_gather(
+// CQ (center_query): p = 1 - theta(q - c, k - c)/pi instead of 1 - theta(q, k - c)/pi.
+// Per row the kernel accumulates q.(k - c) and |k - c|^2 (and, for CQ, c.(k - c)); the
+// logit's q.k is q.(k - c) + q.c with q.c constant per head, and the cosine's numerator
+// q.(k - c) (or (q - c).(k - c) = q.(k - c) - c.(k - c)) is formed without subtracting two
+// large dot products, which keeps it accurate when the keys sit far from the origin
+// (narrow key cones).
+template <typename T, int D, bool CQ>
+__global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) k_attend_gather(
     const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
     const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
     float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
 
   constexpr int NP = VE / 2;  // packed pairs per slice
   uint64_t q2[NP], c2[NP];
-  float qq = 0.f, qc = 0.f;
+  float qq = 0.f, qc = 0.f;  // |q|^2 (CQ: |q - c|^2) and q.c
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
     const float q0 = to_f(q[int64_t(qh) * D + part * VE + 2 * i]);
@@ -331,7 +338,12 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
     const float c1 = center[int64_t(unit) * D + part * VE + 2 * i + 1];
     q2[i] = pk2(q0, q1);
     c2[i] = pk2(c0, c1);
-    qq = fmaf(q0, q0, fmaf(q1, q1, qq));
+    if (CQ) {
+      const float m0 = q0 - c0, m1 = q1 - c1;
+      qq = fmaf(m0, m0, fmaf(m1, m1, qq));
+    } else {
+      qq = fmaf(q0, q0, fmaf(q1, q1, qq));
+    }
     qc = fmaf(q0, c0, fmaf(q1, c1, qc));
   }
 #pragma unroll
@@ -339,7 +351,7 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
     qq += __shfl_xor_sync(0xffffffffu, qq, o);
     qc += __shfl_xor_sync(0xffffffffu, qc, o);
   }
-  const float qnorm = sqrtf(qq);
+  const float qnorm = sqrtf(qq);  // norm of the hashed query
   // this lane's row of the group after reduce_rows8
   const int ju = 4 * ((lane & (LPR / 2)) != 0) + 2 * ((lane & (LPR / 4)) != 0) + ((lane & (LPR / 8)) != 0);
   const float scale = rsqrtf(float(D));
@@ -376,34 +388,39 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
         vv[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    // per row: q.k and |k - c|^2 (q.(k - c) = q.k - q.c), reduced so that every lane
+    // per row: q.(k - c), |k - c|^2 (and c.(k - c) for CQ), reduced so that every lane
     // ends with one row of the group and evaluates the scalar part of its logit
-    float sa[U], sn[U];
+    float sa[U], sn[U], sc[CQ ? U : 1];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       uint64_t k2[NP];
       pairs_of(kv[u], static_cast<const T*>(nullptr), k2);
-      uint64_t a2 = 0ull, n2 = 0ull;
+      uint64_t a2 = 0ull, n2 = 0ull, m2 = 0ull;
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
         const uint64_t d2 = sub2(k2[i], c2[i]);
-        a2 = fma2(q2[i], k2[i], a2);
+        a2 = fma2(q2[i], d2, a2);
         n2 = fma2(d2, d2, n2);
+        if (CQ) m2 = fma2(c2[i], d2, m2);
       }
       sa[u] = lo2(a2) + hi2(a2);
       sn[u] = lo2(n2) + hi2(n2);
+      if (CQ) sc[CQ ? u : 0] = lo2(m2) + hi2(m2);
     }
-    const float rd = reduce_rows8<LPR>(sa, lane);
+    const float rqd = reduce_rows8<LPR>(sa, lane);  // q.(k - c)
     const float rkk = reduce_rows8<LPR>(sn, lane);
+    float rnum = rqd;  // the cosine's numerator: q.(k - c), or (q - c).(k - c)
+    if constexpr (CQ) rnum -= reduce_rows8<LPR>(sc, lane);
     const int je = gi * GR + ju * RPI + sub;
     const uint32_t rent = je < cn ? sl[je] : 0xffffffffu;
     float lg = -CUDART_INF_F;
     if (rent != 0xffffffffu) {
-      lg = rd * scale;
+      lg = (rqd + qc) * scale;  // q.k / sqrt(d)
       if (!(rent & kExactFlag)) {
-        // p = 1 - theta(q, k - c)/pi, u = P[Bin(L, p^K) >= threshold]  (Eq. 10/11)
+        // p = 1 - theta(q, k - c)/pi (CQ: theta(q - c, k - c)), u = P[Bin(L, p^K) >= threshold]
+        // (Eq. 10/11)
         const float kn = sqrtf(rkk);
-        float cs = (qnorm > 0.f && kn > 0.f) ? (rd - qc) / (qnorm * kn) : 0.f;
+        float cs = (qnorm > 0.f && kn > 0.f) ? rnum / (qnorm * kn) : 0.f;
         cs = fminf(1.f, fmaxf(-1.f, cs));
         const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
         // x = p^K by squaring (K <= 12)
@@ -528,22 +545,27 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool CQ>
 static cudaError_t launch_attend_t(const Geometry& g, int splits, const TablesPtrs& t, const void* keys,
                                    const void* values, const void* q, float* out, const DecodePtrs& dp,
                                    cudaStream_t st) {
-  // persistent grid: as many CTAs as can be resident at once, each walking items
-  static int per_sm[64] = {0};
+  // persistent grid: as many CTAs as can be resident at once, each walking items. The
+  // resident count per SM is cached per device; callers on several host threads may fill
+  // the cache at once, each writing the same value.
+  static std::atomic<int> per_sm[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  int& occ = per_sm[dev & 63];
-  if (occ == 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attend_gather<T, D>, kAttThreads, 0) !=
-                       cudaSuccess ||
-                   occ < 1))
-    occ = 1;
+  int occ = per_sm[dev & 63].load(std::memory_order_relaxed);
+  if (occ == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_attend_gather<T, D, CQ>, kAttThreads, 0) !=
+            cudaSuccess ||
+        occ < 1)
+      occ = 1;
+    per_sm[dev & 63].store(occ, std::memory_order_relaxed);
+  }
   const int64_t items = int64_t(splits) * g.queries;
   const int grid = int(std::min<int64_t>(items, int64_t(occ) * device_sm_count()));
-  k_attend_gather<T, D><<<grid, kAttThreads, 0, st>>>(
+  k_attend_gather<T, D, CQ><<<grid, kAttThreads, 0, st>>>(
       dp.lists, dp.list_len, t.center, static_cast<const T*>(keys), static_cast<const T*>(values),
       static_cast<const T*>(q), out, dp.partials, dp.counters, g.cap, g.group, g.K, g.L, g.threshold, splits,
       g.queries);
@@ -554,12 +576,20 @@ cudaError_t launch_attend(const Geometry& g, int n, int splits, const TablesPtrs
                           const void* values, const void* q, float* out, const DecodePtrs& dp,
                           cudaStream_t st) {
   (void)n;
-  if (g.dtype == MP_DTYPE_BF16) {
-    if (g.d == 128) return launch_attend_t<__nv_bfloat16, 128>(g, splits, t, keys, values, q, out, dp, st);
-    return launch_attend_t<__nv_bfloat16, 64>(g, splits, t, keys, values, q, out, dp, st);
+  if (g.center_query) {
+    if (g.dtype == MP_DTYPE_BF16) {
+      if (g.d == 128) return launch_attend_t<__nv_bfloat16, 128, true>(g, splits, t, keys, values, q, out, dp, st);
+      return launch_attend_t<__nv_bfloat16, 64, true>(g, splits, t, keys, values, q, out, dp, st);
+    }
+    if (g.d == 128) return launch_attend_t<float, 128, true>(g, splits, t, keys, values, q, out, dp, st);
+    return launch_attend_t<float, 64, true>(g, splits, t, keys, values, q, out, dp, st);
   }
-  if (g.d == 128) return launch_attend_t<float, 128>(g, splits, t, keys, values, q, out, dp, st);
-  return launch_attend_t<float, 64>(g, splits, t, keys, values, q, out, dp, st);
+  if (g.dtype == MP_DTYPE_BF16) {
+    if (g.d == 128) return launch_attend_t<__nv_bfloat16, 128, false>(g, splits, t, keys, values, q, out, dp, st);
+    return launch_attend_t<__nv_bfloat16, 64, false>(g, splits, t, keys, values, q, out, dp, st);
+  }
+  if (g.d == 128) return launch_attend_t<float, 128, false>(g, splits, t, keys, values, q, out, dp, st);
+  return launch_attend_t<float, 64, false>(g, splits, t, keys, values, q, out, dp, st);
 }
 
 }  // namespace mp

@@ -423,11 +423,14 @@ struct RowsTcArgs {
   int nr;            // rows per CTA (multiple of 32, <= 256)
   int groups_per_w;  // group g uses W matrix g / groups_per_w
   int w_rows;        // W rows between consecutive W matrices (0: shared)
-  const float* negbeta;  // appended keys: -beta [U][kltc] (nullptr: queries)
+  const float* negbeta;  // -beta [U][kltc] added to row r of group g: unit (g * rows + r) / nb_div
+                         // (nullptr: rows hashed as they are)
+  int nb_div;
   int kltc;
   uint16_t* out;
   int64_t out_gs, out_rs, out_ts;
-  DevHeader* hdr;    // status word; appends also raise the appended end to mark_pos + 1
+  DevHeader* hdr;    // status word
+  int mark;          // appends: raise the appended end to mark_pos + 1
   int mark_pos;
 };
 
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
     mbar_init(mdone, 1);
     *abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (a.negbeta && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    if (a.mark && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
       if (a.hdr->magic != kMagic) atomicOr(&a.hdr->status, MP_STATUS_NOT_BUILT);
       else atomicMax(&a.hdr->appended_end, a.mark_pos + 1);
     }
@@ -509,22 +512,31 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   }
   __syncwarp();
   // epilogue: all warps. -beta of the first 32 rows is fetched before the wait for the
-  // accumulator (it does not depend on it)
+  // accumulator (it does not depend on it). Row j of chunk ch is row r0 + 32 ch + j of
+  // group g, centered with unit (g * rows + r0 + 32 ch + j) / nb_div, walked as a
+  // quotient and remainder so that no division runs per row.
   const int h = warp >> 2, quarter = warp & 3;
   const int col = h * 128 + quarter * 32 + lane;  // column within the 256-column tile
-  const float* nbc =
-      a.negbeta ? a.negbeta + (int64_t(g) * a.rows + r0) * a.kltc + int64_t(n) * 256 + col : nullptr;
+  const float* nbc = a.negbeta ? a.negbeta + int64_t(n) * 256 + col : nullptr;
+  const int row_base = g * a.rows + r0;
+  int nb_unit = row_base / a.nb_div, nb_rem = row_base - nb_unit * a.nb_div;
   float nb[32];
+  auto fetch_nb = [&](int ch) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) nb[j] = (nbc && j < nvalid) ? __ldg(nbc + int64_t(j) * a.kltc) : 0.f;
+    for (int j = 0; j < 32; ++j) {
+      nb[j] = (nbc && ch * 32 + j < nvalid) ? __ldg(nbc + int64_t(nb_unit) * a.kltc) : 0.f;
+      if (++nb_rem == a.nb_div) {
+        nb_rem = 0;
+        ++nb_unit;
+      }
+    }
+  };
+  fetch_nb(0);
   const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort));
   if (ok) {
     fence_after();
     for (int ch = 0; ch < (nvalid + 31) / 32; ++ch) {
-      if (ch > 0)
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          nb[j] = (nbc && ch * 32 + j < nvalid) ? __ldg(nbc + int64_t(ch * 32 + j) * a.kltc) : 0.f;
+      if (ch > 0) fetch_nb(ch);
       uint32_t r[32];
       tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * nr + ch * 32), r);
       tmem_wait_ld();
@@ -628,12 +640,14 @@ cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t 
   a.groups_per_w = h.groups_per_w;
   a.w_rows = g.w_per_layer ? 3 * g.kltc : 0;
   a.negbeta = h.negbeta;
+  a.nb_div = h.nb_div > 0 ? h.nb_div : 1;
   a.kltc = g.kltc;
   a.out = h.out;
   a.out_gs = h.out_gs;
   a.out_rs = h.out_rs;
   a.out_ts = h.out_ts;
   a.hdr = h.hdr;
+  a.mark = h.mark;
   a.mark_pos = h.mark_pos;
   CUtensorMap mw, mx;
   if (!make_map(&mw, h.wt16, uint64_t(g.d), uint64_t(g.n_w) * 3 * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||

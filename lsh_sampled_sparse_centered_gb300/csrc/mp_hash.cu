@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kHashCols) k_hash_rows(HashRowsArgs a, int d, 
     float v = 0.f;
     if (r0 + r < a.rows) {
       v = to_f(src[int64_t(a.row0 + r0 + r) * a.src_rs + dim]);
-      if (a.center) v -= a.center[(int64_t(g) * a.c_gs + int64_t(r0 + r) * a.c_rs) * d + dim];
+      if (a.center) v -= a.center[(int64_t(g) * a.c_gs + int64_t((r0 + r) / a.c_div) * a.c_rs) * d + dim];
     }
     xs[i] = v;
   }

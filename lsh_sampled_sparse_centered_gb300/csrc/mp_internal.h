@@ -34,6 +34,7 @@ static_assert(sizeof(DevHeader) == 256, "header size");
 struct Geometry {
   int layers, batch, kvh, qh, d, K, L, s, w, cap, dtype, w_per_layer, threshold;
   int no_center;  // 1: keys hashed uncentered (c = 0)
+  int center_query;  // 1: queries hashed as q - c and p taken from cos(q - c, k - c)
   int group;    // q_heads / kv_heads
   int units;    // layers * batch * kv_heads
   int queries;  // layers * batch * q_heads
@@ -76,7 +77,8 @@ struct DecodePtrs {
 
 // Rows to hash: row r (0-based) of group g lives at
 //   src + g*src_gs + (row0 + r)*src_rs          (elements)
-// and is centered with  center + (g*c_gs + r*c_rs)*d  (if center != nullptr).
+// and is centered with  center + (g*c_gs + (r / c_div)*c_rs)*d  (if center != nullptr;
+// c_div > 1 when several rows share a center, e.g. the query heads of a KV head).
 // Codes go to out + g*out_gs + (row0 + r)*out_rs + t*out_ts.
 struct HashRowsArgs {
   const void* src;
@@ -84,6 +86,7 @@ struct HashRowsArgs {
   int rows, groups, row0;
   const float* center;
   int64_t c_gs, c_rs;
+  int c_div;
   const void* wt;         // [n_w][kltc][d], tile-aligned column order: bf16 (bf16 configs) or fp32
   int64_t w_stride;       // elements between consecutive W matrices (0: shared)
   int groups_per_w;       // group g uses W matrix g / groups_per_w
@@ -95,18 +98,21 @@ struct HashRowsArgs {
 
 // Rows hashed on the tensor cores (bf16 rows and W, d = 64 or 128): `groups` groups of
 // `rows` rows, row r of group g at x + (g * rows + r) * x_rs elements; group g uses W
-// matrix g / groups_per_w (when W is per layer). negbeta != nullptr: the rows are keys
-// of units g * rows + r, centered by adding -beta in the epilogue, and the launch also
-// raises the appended end to mark_pos + 1.
+// matrix g / groups_per_w (when W is per layer). negbeta != nullptr: row r of group g is
+// centered by adding the -beta of unit (g * rows + r) / nb_div in the epilogue (appended
+// keys: nb_div = 1; queries: nb_div = the query heads per KV head). mark != 0: the launch
+// also raises the appended end to mark_pos + 1 (appends).
 struct RowsHashTc {
   const __nv_bfloat16* x;
   int64_t x_rs;
   int rows, groups, groups_per_w;
   const __nv_bfloat16* wt16;
   const float* negbeta;  // [U][kltc]
+  int nb_div;
   uint16_t* out;
   int64_t out_gs, out_rs, out_ts;
   DevHeader* hdr;
+  int mark;
   int mark_pos;
 };
 

@@ -11,7 +11,10 @@
 // GPU that loads the library keeps it resident until the process exits. Host code
 // cannot use the array's name as a device address, so the first call on each device
 // asks the runtime for the address (cudaGetSymbolAddress, with that device current)
-// and caches it. All calls share the array and it keeps the previous call's
+// and caches it for the life of the process. The cache assumes the device's primary
+// context is never torn down: after cudaDeviceReset the module is loaded again and the
+// array can sit at another address, so a process that resets a device must not call
+// this entry point afterwards. All calls share the array and it keeps the previous call's
 // contents; the only words that must start at zero, the split-K completion
 // counters, are reset on the device by the first kernel of every call. Two calls
 // whose kernels overlap on the GPU (different streams, or different host threads

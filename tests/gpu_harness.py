@@ -10,21 +10,23 @@ import oracle as O
 import workloads as WL
 
 
-def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0, centering: bool = True):
+def config_for(mp, wl: WL.Workload, threshold: int = 2, match_mode: int = 0, centering: bool = True,
+               center_query: bool = False):
     return mp.make_config(layers=wl.layers, batch=wl.batch, kv_heads=wl.kv_heads, q_heads=wl.q_heads,
                           head_dim=wl.head_dim, K=wl.K, L=wl.L, n_sink=wl.n_sink, window=wl.window,
                           capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer,
-                          threshold=threshold, match_mode=match_mode, centering=centering)
+                          threshold=threshold, match_mode=match_mode, centering=centering,
+                          center_query=center_query)
 
 
 class DeviceRun:
     """Buffers and calls for one workload on one device."""
 
     def __init__(self, mp, wl: WL.Workload, tensors: dict, device, threshold: int = 2, match_mode: int = 0,
-                 centering: bool = True):
+                 centering: bool = True, center_query: bool = False):
         self.mp, self.wl, self.dev = mp, wl, torch.device(device)
         self.threshold = threshold
-        self.cfg = config_for(mp, wl, threshold, match_mode, centering)
+        self.cfg = config_for(mp, wl, threshold, match_mode, centering, center_query)
         self.tl = mp.mp_tables_layout_get(self.cfg)
         self.dl = mp.mp_decode_layout_get(self.cfg)
         self.tables = torch.empty(self.tl.total_bytes, dtype=torch.uint8, device=self.dev)
@@ -186,10 +188,12 @@ def check_planes(planes: np.ndarray, codes: np.ndarray, n: int, K: int) -> None:
 
 def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshold: int = 2,
                    units=None, qheads=None, steps=None, check_csr_tables: int = 8, tol: float = 2e-3,
-                   match_mode: int = 0, centering: bool = True) -> dict:
+                   match_mode: int = 0, centering: bool = True, center_query: bool = False) -> dict:
     """Build, append and decode `wl` through the C ABI and compare every stage with the
-    oracle on the chosen units / query heads / steps. Returns counters for reporting."""
-    run = DeviceRun(mp, wl, tensors, device, threshold, match_mode, centering)
+    oracle on the chosen units / query heads / steps. With center_query the query is
+    hashed as q - c and p is the collision probability of q - c with k - c (the oracle's
+    other reading). Returns counters for reporting."""
+    run = DeviceRun(mp, wl, tensors, device, threshold, match_mode, centering, center_query)
     run.build()
     torch.cuda.synchronize()
     # the W status bit is informational (the tensor-core paths then use W's three-term split)
@@ -260,9 +264,10 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
                     continue
                 qi = q_index(wl, l, b, j)
                 q64 = tensors["queries"][step, l, b, j].double().cpu().numpy()
+                qh64 = q64 - tab.center if center_query else q64   # the hashed query
                 W64 = tab.W
-                qref = O.simhash_codes(q64[None, :], W64, wl.K, wl.L)[0]
-                qtie = tie_codes(O.near_ties(q64[None, :], W64), wl.K, wl.L)[0]
+                qref = O.simhash_codes(qh64[None, :], W64, wl.K, wl.L)[0]
+                qtie = tie_codes(O.near_ties(qh64[None, :], W64), wl.K, wl.L)[0]
                 cq = compare_codes(qc[qi][None, :], qref[None, :], qtie[None, :])
                 assert cq["bad"] == 0, ("query", qi, cq)
                 rep["q_codes_differ"] += cq["differ"]
@@ -276,14 +281,14 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
                 assert np.all(lst[nsq:] & mp.EXACT_FLAG)
                 np.testing.assert_array_equal(lst[nsq:] & ~mp.EXACT_FLAG, T_ref)
                 # attention given S (oracle u, fp64) vs GPU output
-                p = O.collision_probability(q64, k64[S_ref] - tab.center[None, :])
+                p = O.collision_probability(qh64, k64[S_ref] - tab.center[None, :])
                 uS = O.inclusion_probability(p, wl.K, wl.L, threshold)
                 o_ref = O.snis_attention(q64, k64, v64, S_ref, uS, T_ref)
                 err = rel_l2(out[l, b, j], o_ref)
                 assert err < tol, ("output", qi, err)
                 rep["max_rel_l2"] = max(rep["max_rel_l2"], err)
                 # the oracle end to end, with its own codes
-                r = O.decode_head(q64, k64, v64, tab, n, wl.window, threshold)
+                r = O.decode_head(q64, k64, v64, tab, n, wl.window, threshold, center_query=center_query)
                 if not np.array_equal(r["S"], S_ref):
                     rep["S_differ_oracle_codes"] += 1
                     assert cq["differ"] > 0 or rep["codes_differ"] > 0, ("S differs without ties", qi)

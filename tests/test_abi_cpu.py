@@ -64,8 +64,9 @@ def test_config_validation(mp):
     c = _cfg(mp)
     c.no_centering = 2
     assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG
-    # the centered-query reading is not built on the CUDA path yet
-    assert mp.mp_config_check(_cfg(mp, center_query=True)) == mp.MP_ERR_UNSUPPORTED
+    # both query readings are accepted, with and without key centering
+    assert mp.mp_config_check(_cfg(mp, center_query=True)) == mp.MP_OK
+    assert mp.mp_config_check(_cfg(mp, center_query=True, centering=False)) == mp.MP_OK
     c = _cfg(mp)
     c.center_query = 2
     assert mp.mp_config_check(c) == mp.MP_ERR_INVALID_ARG

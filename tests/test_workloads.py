@@ -34,6 +34,24 @@ def test_cone_geometry_of_keys_and_queries():
     assert abs((q[8:12] @ mu).mean().item() + 2.0) < 2.0
 
 
+def test_tight_cone_and_constant_keys():
+    """The tight-cone recipe puts the keys at cosine ~a/sqrt(a^2 + d) from mu and the sink
+    at -sink_scale·a·mu; constant keys are a·mu exactly."""
+    wl = WL.WORKLOADS[1].replace(cone=40.0, sink_scale=1.0)
+    mu = WL.head_mu(wl, 0, 0, 5)
+    k = WL.keys_block(wl, 0, 0, 5, 0, 4000)
+    assert torch.allclose(k[0], -40.0 * mu)
+    cos = (k[1:] @ mu) / torch.linalg.vector_norm(k[1:], dim=1)
+    assert abs(cos.mean().item() - 40.0 / math.sqrt(40.0 ** 2 + 128)) < 0.01
+    # pairwise cosine of two keys: about a^2 / (a^2 + d)
+    kk = k[1:2001] / torch.linalg.vector_norm(k[1:2001], dim=1, keepdim=True)
+    pair = (kk[:1000] * kk[1000:]).sum(dim=1).mean().item()
+    assert abs(pair - 1600.0 / (1600.0 + 128)) < 0.01
+    c = WL.keys_block(wl.replace(constant_keys=True), 0, 0, 5, 0, 50)
+    assert torch.equal(c[1:], (40.0 * mu)[None, :].expand(49, -1))
+    assert torch.allclose(c[0], -40.0 * mu)
+
+
 def test_generate_shapes_and_dtypes():
     wl = WL.WORKLOADS[0]
     t = WL.generate(wl)
@@ -77,7 +95,9 @@ def test_generate_equals_the_block_functions():
              WL.Workload("mix", layers=2, batch=2, kv_heads=3, q_heads=6, head_dim=128, n_prefill=1037,
                          steps=5, append=True, K=6, L=20, dtype="bf16", seed=17, iso_fraction=0.1,
                          w_per_layer=True),
-             WL.WORKLOADS[1].replace(n_prefill=3000, steps=3)]
+             WL.WORKLOADS[1].replace(n_prefill=3000, steps=3),
+             WL.WORKLOADS[1].replace(n_prefill=700, steps=2, cone=40.0, sink_scale=1.0),
+             WL.WORKLOADS[0].replace(n_prefill=300, constant_keys=True)]
     for wl in cases:
         t = WL.generate(wl)
         k, v, q = _generate_block_by_block(wl)

@@ -12,10 +12,15 @@ inside int64 without overflow so that CPU and CUDA tensors give the same integer
 
 Geometry of the synthetic data follows the attention geometry described in
 "MagicPIG: LSH Sampling for Efficient LLM Generation" (arXiv 2410.16179v2), §3.1 and
-Figure 2c: keys in a narrow cone (k = 3·mu + N(0, I)), the sink key almost opposite
-(k_0 = -6·mu) and queries on the sink's side (q = -2·mu + N(0, I)); values N(0, 1).
-The projection matrix W has the shape d x (K·L) given in Algorithm 1 of the same
-page, drawn N(0, 1).
+Figure 2c: keys in a cone around a direction mu (k = a·mu + N(0, I), a = ``cone``,
+3 by default), the sink key opposite (k_0 = -sink_scale·a·mu, -6·mu by default) and
+queries on the sink's side (q = -2·mu + N(0, I)); values N(0, 1). How narrow the cone
+is, the pages leave open beyond "almost identical" key directions (§3.1, Figure 5a:
+cosine above 0.99 between keys); a = 40 to 80 at d = 128 gives cos(k, mu) of 0.96 to
+0.99 (the tight-cone recipe). ``constant_keys`` draws every key but the sink as a·mu
+exactly (no noise), the degenerate head in which every centered key is zero. The
+projection matrix W has the shape d x (K·L) given in Algorithm 1 of the same page,
+drawn N(0, 1).
 """
 from __future__ import annotations
 
@@ -61,6 +66,9 @@ class Workload:
     n_sink: int = 4
     window: int = 64
     iso_fraction: float = 0.0   # share of keys drawn isotropic N(0, I) instead of from the cone
+    cone: float = 3.0           # a in k = a·mu + N(0, I)
+    sink_scale: float = 2.0     # the sink key is -sink_scale·a·mu
+    constant_keys: bool = False  # every key but the sink is a·mu exactly (no noise)
     w_per_layer: bool = False
     w_bf16: bool = True         # W rounded to bf16-representable values
 
@@ -218,12 +226,12 @@ def keys_block(wl: Workload, layer: int, b: int, h: int, t0: int, t1: int,
     mu = head_mu(wl, layer, b, h, device)
     noise = gaussian(stream_key(wl.seed, P_KEY, layer, b, h), n * d, device,
                      offset=t0 * d).view(n, d)
-    k = noise + 3.0 * mu
+    k = wl.cone * mu + (0.0 * noise if wl.constant_keys else noise)
     if wl.iso_fraction > 0.0:
         pick = uniform(stream_key(wl.seed, P_MIX, layer, b, h), n, device, offset=t0)
         k = torch.where((pick < wl.iso_fraction)[:, None], noise, k)
     if t0 == 0 and n > 0:
-        k[0] = -6.0 * mu
+        k[0] = -(wl.sink_scale * wl.cone) * mu
     return k
 
 
@@ -280,12 +288,12 @@ def generate(wl: Workload, device="cpu", layers: Optional[list[int]] = None,
             mus = torch.stack([head_mu(wl, l, b, h, device) for h in range(H)])
             noise = gaussian_streams([stream_key(wl.seed, P_KEY, l, b, h) for h in range(H)], cap * d,
                                      device).view(H, cap, d)
-            k = noise + 3.0 * mus[:, None, :]
+            k = wl.cone * mus[:, None, :] + (0.0 * noise if wl.constant_keys else noise)
             if wl.iso_fraction > 0.0:
                 pick = uniform_streams([stream_key(wl.seed, P_MIX, l, b, h) for h in range(H)], cap, device)
                 k = torch.where((pick < wl.iso_fraction)[:, :, None], noise, k)
             if cap > 0:
-                k[:, 0] = -6.0 * mus
+                k[:, 0] = -(wl.sink_scale * wl.cone) * mus
             keys[l, b] = round_to(k, wl.dtype)
             del noise, k
             if with_values:
