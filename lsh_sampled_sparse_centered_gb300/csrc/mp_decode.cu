@@ -22,6 +22,7 @@ namespace mp {
 // [n_sink, n - window); with threshold 1 it is seen1. Compaction writes S in
 // ascending token order, then the exact tokens (bit 31 set).
 constexpr int kMatchWarps = 8;
+constexpr int kMatchUnroll = 4;  // rounds of 32 ids per warp in flight
 
 __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
@@ -81,49 +82,55 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
     }
     __syncthreads();
     const uint16_t* idu = ids + tbase * cap;
-    // Each thread walks whole buckets (bucket p = thread, thread + 256, ...): the ids are
-    // read as 16-byte aligned chunks of 8, two chunks in flight, and every id is marked
-    // by the thread itself, so all lanes do useful work whatever the bucket sizes. Within
-    // a group of two chunks the first marks are all issued before the second ones, so
-    // that the atomics do not wait on one another.
-    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-      const uint2 e = bkt[p];
-      const uint32_t sz = e.y & 0xffffu, tok0 = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
-      const uintptr_t a0 = reinterpret_cast<uintptr_t>(idu + e.x);
-      const uint32_t skip = uint32_t(a0 & 15u) >> 1;  // ids of the first chunk before the bucket
-      const uint4* ch = reinterpret_cast<const uint4*>(a0 & ~uintptr_t(15));
-      const uint32_t nch = (skip + sz + 7u) >> 3;
-      for (uint32_t c0 = 0; c0 < nch; c0 += 2) {
-        uint4 v[2];
+    // Warp-cooperative walk. Warp w takes tables w, w + 8, ...; the runs of those tables
+    // (one per segment, table-major) are concatenated, and in every round the 32 lanes
+    // take 32 consecutive positions of that sequence, so a warp instruction covers 32 ids
+    // whatever the run lengths. kMatchUnroll rounds of id loads are issued before their
+    // marks, and within them all first marks before the dependent second ones. Each lane
+    // keeps a cursor (run index, the run's table and segment, the position of its first
+    // id) that only moves forward.
+    {
+      const int my_runs = ((L - warp + kMatchWarps - 1) / kMatchWarps) * nsu;
+      int r = 0, tk = warp, sg = 0;
+      uint32_t rbeg = 0;
+      uint2 e = my_runs > 0 ? bkt[warp * nsu] : make_uint2(0u, 0u);
+      uint32_t pos = uint32_t(lane);
+      while (__any_sync(0xffffffffu, r < my_runs)) {
+        uint32_t tok[kMatchUnroll], addr[kMatchUnroll];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) v[k] = c0 + k < nch ? __ldg(ch + c0 + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kMatchUnroll; ++u) {
+          while (r < my_runs && pos - rbeg >= (e.y & 0xffffu)) {
+            rbeg += e.y & 0xffffu;
+            ++r;
+            if (++sg == nsu) {
+              sg = 0;
+              tk += kMatchWarps;
+            }
+            if (r < my_runs) e = bkt[tk * nsu + sg];
+          }
+          addr[u] = r < my_runs ? e.x + (pos - rbeg) : 0xffffffffu;
+          tok[u] = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
+          pos += 32u;
+        }
+#pragma unroll
+        for (int u = 0; u < kMatchUnroll; ++u)
+          tok[u] = addr[u] != 0xffffffffu ? tok[u] + __ldg(idu + addr[u]) : 0xffffffffu;
         uint32_t dup = 0;
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t word = (q < 2) ? v[k].x : (q < 4) ? v[k].y : (q < 6) ? v[k].z : v[k].w;
-            const uint32_t i = (c0 + k) * 8u + uint32_t(q) - skip;  // index in the bucket (wraps if < 0)
-            const uint32_t tok = tok0 + ((word >> (16 * (q & 1))) & 0xffffu);
-            if (i < sz && tok < uint32_t(hi)) {
-              if (bytes) {
-                atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
-              } else {
-                const uint32_t bit = 1u << (tok & 31);
-                if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1u << (k * 8 + q);
-              }
+        for (int u = 0; u < kMatchUnroll; ++u) {
+          if (tok[u] < uint32_t(hi)) {
+            if (bytes) {
+              atomicAdd(&cnt[tok[u] >> 2], 1u << (8 * (tok[u] & 3)));
+            } else {
+              const uint32_t bit = 1u << (tok[u] & 31);
+              if (atomicOr(&seen1[tok[u] >> 5], bit) & bit) dup |= 1u << u;
             }
           }
+        }
         if (dup) {
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if ((dup >> (k * 8 + q)) & 1u) {
-                const uint32_t word = (q < 2) ? v[k].x : (q < 4) ? v[k].y : (q < 6) ? v[k].z : v[k].w;
-                const uint32_t tok = tok0 + ((word >> (16 * (q & 1))) & 0xffffu);
-                atomicOr(&seen2[tok >> 5], 1u << (tok & 31));
-              }
+          for (int u = 0; u < kMatchUnroll; ++u)
+            if ((dup >> u) & 1u) atomicOr(&seen2[tok[u] >> 5], 1u << (tok[u] & 31));
         }
       }
     }
