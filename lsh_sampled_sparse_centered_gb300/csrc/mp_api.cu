@@ -48,11 +48,11 @@ static int check_config(const mp_config* c) {
   if (c->threshold > 2 && resolve_match(c) == MP_MATCH_CSR && c->capacity > kMaxCapacityCounters)
     return MP_ERR_UNSUPPORTED;
   if (resolve_match(c) == MP_MATCH_CSR) {
-    // the match kernel keeps per-token bitmaps (or byte counters) and one bucket range
-    // per (table, 32768-token segment) in shared memory
+    // the match kernel keeps per-token bitmaps (or byte counters), one bucket run and
+    // its chunk prefix per (table, 32768-token segment) and the query codes in shared memory
     const int64_t words = (int64_t(c->capacity) + 31) / 32;
     const int64_t nseg = (int64_t(c->capacity) + kCsrSeg - 1) / kCsrSeg;
-    const int64_t smem = words * 4 * (c->threshold > 2 ? 9 : 2) + int64_t(c->L) * (nseg * 8 + 2) + 20;
+    const int64_t smem = words * 4 * (c->threshold > 2 ? 9 : 2) + int64_t(c->L) * (nseg * 12 + 2) + 24;
     if (smem > 227 * 1024) return MP_ERR_UNSUPPORTED;
   }
   // grid limits: units and queries index blockIdx.x / y

@@ -22,9 +22,41 @@ namespace mp {
 // [n_sink, n - window); with threshold 1 it is seen1. Compaction writes S in
 // ascending token order, then the exact tokens (bit 31 set).
 constexpr int kMatchWarps = 8;
-constexpr int kMatchUnroll = 4;  // rounds of 32 ids per warp in flight
+constexpr int kChunkUnroll = 4;  // 16-byte chunks of ids in flight per thread
 
-__global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hdr,
+// Exclusive scan of v[0..n) in place by the whole block; v[n] receives the total.
+__device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {
+  __shared__ uint32_t wsum[kMatchWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = min(n, int(threadIdx.x) * per), i1 = min(n, i0 + per);
+  uint32_t local = 0;
+  for (int i = i0; i < i1; ++i) local += v[i];
+  uint32_t x = local;
+#pragma unroll
+  for (int k = 1; k < 32; k <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, k);
+    if (lane >= k) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  uint32_t before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kMatchWarps; ++w) {
+    before += (w < warp) ? wsum[w] : 0u;
+    total += wsum[w];
+  }
+  uint32_t run = before + x - local;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t c = v[i];
+    v[i] = run;
+    run += c;
+  }
+  if (threadIdx.x == 0) v[n] = total;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
                                                    const uint16_t* __restrict__ off,
@@ -45,8 +77,9 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
   uint32_t* seen2 = sm + nwords;
   uint32_t* cnt = sm + nwords;  // [nwords * 8] byte counters (threshold >= 3)
   const int body = bytes ? nwords * 9 : nwords * 2;
-  uint2* bkt = reinterpret_cast<uint2*>(sm + ((body + 1) & ~1));  // [L * nseg] bucket ranges
-  uint16_t* qc = reinterpret_cast<uint16_t*>(bkt + L * nseg);
+  uint2* bkt = reinterpret_cast<uint2*>(sm + ((body + 1) & ~1));  // [L * nseg] runs of ids
+  uint32_t* pre = reinterpret_cast<uint32_t*>(bkt + L * nseg);     // [L * nseg + 1] chunk prefix
+  uint16_t* qc = reinterpret_cast<uint16_t*>(pre + L * nseg + 1);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   const bool built = hdr->magic == kMagic;
@@ -64,73 +97,91 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
   __syncthreads();
 
   if (built && hi > lo) {
-    // tokens hashed at build time: the query's bucket in every (table, segment). The
-    // bucket ranges are fetched first, one table per thread (the starts of a bucket in
-    // all segments and those of the next bucket share a cache line), then the ids.
+    // Tokens hashed at build time: the query's bucket in every (table, segment), one run
+    // of ids each. Every run is covered by the 16-byte chunks that hold it; the chunks of
+    // all runs of the head are numbered consecutively (a block scan of the per-run chunk
+    // counts) and split evenly over the threads, so each thread has about the same number
+    // of chunks, reads them kChunkUnroll at a time (all loads in flight before their
+    // marks) and marks every id of a chunk itself.
     const int64_t tbase = int64_t(unit) * L;
     const int lo_b = min(s, n0);  // first token bucketed at build time
     const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
-    const int pairs = L * nsu;
+    const int runs = L * nsu;
+    const uintptr_t idb = reinterpret_cast<uintptr_t>(ids + tbase * cap);  // the unit's id arrays
+    const uintptr_t idb16 = idb & ~uintptr_t(15);
+    // run r = t * nsu + sg: {first chunk (16-byte units from idb16), size | skip << 16 | sg << 19},
+    // skip = ids of the first chunk before the run; pre[r] = chunks of runs before r
     for (int t = threadIdx.x; t < L; t += blockDim.x) {
       const uint16_t* o = off + (tbase + t) * int64_t(nb + 1) * nseg + int64_t(qc[t]) * nseg;
       for (int sg = 0; sg < nsu; ++sg) {
         const uint32_t b0 = __ldg(o + sg), b1 = __ldg(o + nseg + sg);
-        // {position of the bucket in the unit's id arrays, size | segment << 16}
-        bkt[t * nsu + sg] =
-            make_uint2(uint32_t(t) * uint32_t(cap) + uint32_t(sg) * kCsrSeg + b0, (b1 - b0) | (uint32_t(sg) << 16));
+        const uint32_t sz = b1 - b0;
+        const uintptr_t a = idb + 2u * (uint64_t(t) * uint64_t(cap) + uint64_t(sg) * kCsrSeg + b0);
+        const uint32_t c0 = uint32_t((a - idb16) >> 4);
+        bkt[t * nsu + sg] = make_uint2(c0, sz | (uint32_t((a & 15u) >> 1) << 16) | (uint32_t(sg) << 19));
+        pre[t * nsu + sg] = sz ? uint32_t(((a + 2u * sz - 1u) >> 4) - (a >> 4) + 1u) : 0u;
       }
     }
     __syncthreads();
-    const uint16_t* idu = ids + tbase * cap;
-    // Warp-cooperative walk. Warp w takes tables w, w + 8, ...; the runs of those tables
-    // (one per segment, table-major) are concatenated, and in every round the 32 lanes
-    // take 32 consecutive positions of that sequence, so a warp instruction covers 32 ids
-    // whatever the run lengths. kMatchUnroll rounds of id loads are issued before their
-    // marks, and within them all first marks before the dependent second ones. Each lane
-    // keeps a cursor (run index, the run's table and segment, the position of its first
-    // id) that only moves forward.
-    {
-      const int my_runs = ((L - warp + kMatchWarps - 1) / kMatchWarps) * nsu;
-      int r = 0, tk = warp, sg = 0;
-      uint32_t rbeg = 0;
-      uint2 e = my_runs > 0 ? bkt[warp * nsu] : make_uint2(0u, 0u);
-      uint32_t pos = uint32_t(lane);
-      while (__any_sync(0xffffffffu, r < my_runs)) {
-        uint32_t tok[kMatchUnroll], addr[kMatchUnroll];
+    block_exclusive_scan(pre, runs);  // pre[runs] = total chunks
+    const uint32_t total = pre[runs];
+    const uint32_t cb = uint32_t((uint64_t(total) * threadIdx.x) / blockDim.x);
+    const uint32_t ce = uint32_t((uint64_t(total) * (threadIdx.x + 1)) / blockDim.x);
+    if (cb < ce) {
+      // the last run r with pre[r] <= cb (then pre[r + 1] > cb)
+      int r = 0, rh = runs;
+      while (rh - r > 1) {
+        const int mid = (r + rh) >> 1;
+        if (pre[mid] <= cb) r = mid;
+        else rh = mid;
+      }
+      const uint4* cbase = reinterpret_cast<const uint4*>(idb16);
+      for (uint32_t c = cb; c < ce; c += kChunkUnroll) {
+        uint4 v[kChunkUnroll];
+        uint32_t tok0[kChunkUnroll], span[kChunkUnroll];  // span: first | end << 8 of the valid ids
 #pragma unroll
-        for (int u = 0; u < kMatchUnroll; ++u) {
-          while (r < my_runs && pos - rbeg >= (e.y & 0xffffu)) {
-            rbeg += e.y & 0xffffu;
-            ++r;
-            if (++sg == nsu) {
-              sg = 0;
-              tk += kMatchWarps;
-            }
-            if (r < my_runs) e = bkt[tk * nsu + sg];
+        for (int u = 0; u < kChunkUnroll; ++u) {
+          const uint32_t cc = c + u;
+          span[u] = 0u;
+          tok0[u] = 0u;
+          v[u] = make_uint4(0u, 0u, 0u, 0u);
+          if (cc < ce) {
+            while (cc >= pre[r + 1]) ++r;
+            const uint2 e = bkt[r];
+            const uint32_t k = cc - pre[r];  // chunk index within the run
+            const int32_t first = int32_t((e.y >> 16) & 7u) - int32_t(8u * k);  // ids before the run
+            const int32_t end = first + int32_t(e.y & 0xffffu);
+            span[u] = uint32_t(max(first, 0)) | (uint32_t(min(end, 8)) << 8);
+            tok0[u] = uint32_t(lo_b) + ((e.y >> 19) & 15u) * kCsrSeg;
+            v[u] = __ldg(cbase + e.x + k);
           }
-          addr[u] = r < my_runs ? e.x + (pos - rbeg) : 0xffffffffu;
-          tok[u] = uint32_t(lo_b) + (e.y >> 16) * kCsrSeg;
-          pos += 32u;
         }
-#pragma unroll
-        for (int u = 0; u < kMatchUnroll; ++u)
-          tok[u] = addr[u] != 0xffffffffu ? tok[u] + __ldg(idu + addr[u]) : 0xffffffffu;
         uint32_t dup = 0;
 #pragma unroll
-        for (int u = 0; u < kMatchUnroll; ++u) {
-          if (tok[u] < uint32_t(hi)) {
-            if (bytes) {
-              atomicAdd(&cnt[tok[u] >> 2], 1u << (8 * (tok[u] & 3)));
-            } else {
-              const uint32_t bit = 1u << (tok[u] & 31);
-              if (atomicOr(&seen1[tok[u] >> 5], bit) & bit) dup |= 1u << u;
+        for (int u = 0; u < kChunkUnroll; ++u)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
+            const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
+            if (uint32_t(q) >= (span[u] & 0xffu) && uint32_t(q) < (span[u] >> 8) && tok < uint32_t(hi)) {
+              if (bytes) {
+                atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
+              } else {
+                const uint32_t bit = 1u << (tok & 31);
+                if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1u << (u * 8 + q);
+              }
             }
           }
-        }
         if (dup) {
 #pragma unroll
-          for (int u = 0; u < kMatchUnroll; ++u)
-            if ((dup >> u) & 1u) atomicOr(&seen2[tok[u] >> 5], 1u << (tok[u] & 31));
+          for (int u = 0; u < kChunkUnroll; ++u)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if ((dup >> (u * 8 + q)) & 1u) {
+                const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
+                const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
+                atomicOr(&seen2[tok >> 5], 1u << (tok & 31));
+              }
         }
       }
     }
@@ -179,7 +230,7 @@ cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, cons
   const int hi = max(lo, n - g.w);
   const int nwords = (hi + 31) >> 5;
   const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
-  const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 8 + size_t(g.L) * 2 + 16;
+  const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 12 + 4 + size_t(g.L) * 2 + 16;
   cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   k_match_csr<<<g.queries, kMatchWarps * 32, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists,
                                                          dp.list_len, dp.sample_count, dp.counters, n, g.s, g.w, g.L,
