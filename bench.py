@@ -193,9 +193,12 @@ class Job:
         for s in range(wl.steps):
             n = wl.seq_len(s)
             if wl.append:
-                mp.mp_append(self.cfg, self.tables, k, n - 1, stream=self.sp)
-            mp.mp_decode_attention(self.cfg, self.tables, k, v, n, qs[s], self.outs[s], self.scratch,
-                                   scratch_bytes=self.dl.total_bytes, stream=self.sp)
+                # append token n - 1 and decode over n tokens: one call, one hashing launch
+                mp.mp_decode_step(self.cfg, self.tables, k, v, n - 1, qs[s], self.outs[s], self.scratch,
+                                  scratch_bytes=self.dl.total_bytes, stream=self.sp)
+            else:
+                mp.mp_decode_attention(self.cfg, self.tables, k, v, n, qs[s], self.outs[s], self.scratch,
+                                       scratch_bytes=self.dl.total_bytes, stream=self.sp)
             if self.hook:
                 self.hook(s, n)
 
@@ -229,9 +232,10 @@ class Job:
 
     @property
     def launches_per_job(self):
-        # prepare_w, center (2 kernels), hash keys, csr build; per step: append hash (it
-        # also marks the appended end), query hash, match, attend
-        return 5 + self.wl.steps * (4 if self.wl.append else 3)
+        # prepare_w, center (2 kernels), hash keys, csr build; per step: one hash launch
+        # (the appended keys, which also marks the appended end, with the queries), match,
+        # attend
+        return 5 + self.wl.steps * 3
 
 
 def decode_state_stats(job, torch):
@@ -371,7 +375,8 @@ def run_ours(args, rank, world, local):
 # kernel -> source file whose contents the recorded DRAM counters belong to
 KERNEL_SOURCE = {
     "attend": "mp_decode.cu", "match_csr": "mp_decode.cu", "hash_keys_tc": "mp_gemm.cu",
-    "hash_query": "mp_gemm.cu", "hash_append": "mp_gemm.cu", "csr_build": "mp_csr.cu", "center": "mp_hash.cu",
+    "hash_query": "mp_gemm.cu", "hash_append": "mp_gemm.cu", "hash_step": "mp_gemm.cu", "csr_build": "mp_csr.cu",
+    "center": "mp_hash.cu",
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -413,6 +418,7 @@ def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
         "hash_keys_simt": ("flops", 2.0 * U * n0 * d * KL),
         "csr_build": ("bytes", U * wl.L * ((n0 - s) * (2 + 2) + -(-(n0 - s) // 32768) * (2 ** wl.K + 1) * 2)),
         "hash_append": ("flops", 2.0 * steps * U * d * KL),
+        "hash_step": ("flops", 2.0 * steps * (U + Q) * d * KL),
         "mark_appended": ("bytes", 0),
         "hash_query": ("flops", 2.0 * steps * Q * d * KL),
         "match_csr": ("bytes", bucket_entries * 2 + steps * Q * wl.L * (4 * -(-(n0 - s) // 32768) + 2)

@@ -211,6 +211,20 @@ MP_API int mp_decode_attention(const mp_config* cfg, void* tables, const void* k
                         const void* values, int32_t n, const void* q, float* out,
                         void* scratch, size_t scratch_bytes, void* stream);
 
+/* One decode step of a growing sequence: mp_append(cfg, tables, keys, pos) followed by
+ * mp_decode_attention(..., n = pos + 1, ...), with the same results, in fewer launches:
+ * the appended key of every (layer, sequence, KV head) and every query are hashed
+ * together (on the tensor cores, one launch that loads each W tile once for both).
+ * This is the step of the pages' decoding loop (Algorithm 1 per generated token, the
+ * new key entering the tables; §4.4): the caller has already written keys[..][pos][:]
+ * and values[..][pos][:].
+ *   pos : the new token, 0 <= pos < capacity (else MP_ERR_CAPACITY); meant to be the
+ *         next token after the prefill and earlier appends (see mp_append).
+ * Other arguments, errors and writes as mp_append and mp_decode_attention. */
+MP_API int mp_decode_step(const mp_config* cfg, void* tables, const void* keys, const void* values,
+                          int32_t pos, const void* q, float* out, void* scratch, size_t scratch_bytes,
+                          void* stream);
+
 /* Size of the scratch array built into the library for mp_decode_attention_static. */
 #define MP_STATIC_SCRATCH_BYTES (32u << 20)
 

@@ -80,6 +80,7 @@ _SIGS = {
     "mp_build_tables": (ctypes.c_int, [_CFG, _P, _I, _P, _P, _P]),
     "mp_append": (ctypes.c_int, [_CFG, _P, _P, _I, _P]),
     "mp_decode_attention": (ctypes.c_int, [_CFG, _P, _P, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mp_decode_step": (ctypes.c_int, [_CFG, _P, _P, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "mp_decode_attention_static": (ctypes.c_int, [_CFG, _P, _P, _P, _I, _P, _P, _P]),
     "mp_get_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "mp_profile_enable": (ctypes.c_int, [ctypes.c_int]),
@@ -181,6 +182,15 @@ def mp_decode_attention(cfg: mp_config, tables, keys, values, n: int, q, out, sc
         scratch_bytes = scratch.numel() * scratch.element_size()
     return _check("mp_decode_attention", _lib.mp_decode_attention(
         ctypes.byref(cfg), _ptr(tables), _ptr(keys), _ptr(values), n, _ptr(q), _ptr(out), _ptr(scratch),
+        scratch_bytes, _stream(stream)))
+
+
+def mp_decode_step(cfg: mp_config, tables, keys, values, pos: int, q, out, scratch,
+                   scratch_bytes: Optional[int] = None, stream=None) -> int:
+    if scratch_bytes is None:
+        scratch_bytes = scratch.numel() * scratch.element_size()
+    return _check("mp_decode_step", _lib.mp_decode_step(
+        ctypes.byref(cfg), _ptr(tables), _ptr(keys), _ptr(values), pos, _ptr(q), _ptr(out), _ptr(scratch),
         scratch_bytes, _stream(stream)))
 
 

@@ -251,12 +251,12 @@ static int choose_splits(const Geometry& g, int n) {
 // ---- optional per-launch event timing ----
 enum KernelId {
   K_PREPARE_W, K_CENTER, K_HASH_KEYS_SIMT, K_HASH_KEYS_TC, K_CSR_BUILD, K_HASH_APPEND, K_MARK_APPENDED,
-  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_PLANES_BUILD, K_PLANES_APPEND, K_SCAN, K_COMPACT, K_COUNT
+  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_PLANES_BUILD, K_PLANES_APPEND, K_SCAN, K_COMPACT, K_HASH_STEP, K_COUNT
 };
 static const char* kKernelNames[K_COUNT] = {"prepare_w", "center", "hash_keys_simt", "hash_keys_tc",
                                             "csr_build", "hash_append", "mark_appended", "hash_query",
                                             "match_csr", "attend", "planes_build", "planes_append",
-                                            "scan", "compact"};
+                                            "scan", "compact", "hash_step"};
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
@@ -406,20 +406,16 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
   return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 
-int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream) {
-  int rc = check_config(cfg);
-  if (rc != MP_OK) return rc;
-  if (!keys || !tables) return MP_ERR_INVALID_ARG;
-  if (!aligned16(keys) || (reinterpret_cast<uintptr_t>(tables) & 255u)) return MP_ERR_INVALID_ARG;
-  if (pos < 0 || pos >= cfg->capacity) return MP_ERR_CAPACITY;
-  if (injected("append")) return MP_ERR_INJECTED;
-  const Geometry g = geometry(cfg);
-  const TablesPtrs t = tables_ptrs(g, tables);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaGetLastError();
+}  // extern "C"
+
+namespace mp {
+
+// Rows of a decode step's append: the key at token `pos` of every (layer, sequence,
+// KV head), one group per layer, centered with its unit's build-time center.
+static HashRowsArgs append_rows_simt(const Geometry& g, const TablesPtrs& t, const void* keys, int pos) {
   HashRowsArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.src = keys;
+  a.src = static_cast<const char*>(keys) + int64_t(pos) * g.d * (g.dtype == MP_DTYPE_BF16 ? 2 : 4);
   a.src_gs = int64_t(g.batch) * g.kvh * g.cap * g.d;  // one group per layer
   a.src_rs = int64_t(g.cap) * g.d;                     // one row per (sequence, KV head)
   a.rows = g.batch * g.kvh;
@@ -432,74 +428,42 @@ int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos,
   a.wt = t.wt32;
   a.w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
   a.groups_per_w = 1;
-  a.out = t.codes;
+  a.out = t.codes + pos;
   a.out_gs = int64_t(g.batch) * g.kvh * g.L * g.cap;
   a.out_rs = int64_t(g.L) * g.cap;
   a.out_ts = g.cap;
-  // the row index addresses (sequence, KV head); the token is `pos`
-  a.src = static_cast<const char*>(keys) + int64_t(pos) * g.d * (g.dtype == MP_DTYPE_BF16 ? 2 : 4);
-  a.out = t.codes + pos;
   // the hash kernel also records the new appended end (no projections when K = 0:
   // then a one-thread kernel does it)
   a.mark_hdr = g.nt > 0 ? t.hdr : nullptr;
   a.mark_pos = pos;
-  if (rows_on_tensor_cores(g, t)) {
-    RowsHashTc h;
-    std::memset(&h, 0, sizeof(h));
-    h.x = static_cast<const __nv_bfloat16*>(keys) + int64_t(pos) * g.d;
-    h.x_rs = int64_t(g.cap) * g.d;
-    h.rows = g.batch * g.kvh;
-    h.groups = g.layers;
-    h.groups_per_w = 1;
-    h.wt16 = t.wt16;
-    h.negbeta = t.negbeta;
-    h.nb_div = 1;
-    h.out = t.codes + pos;
-    h.out_gs = a.out_gs;
-    h.out_rs = a.out_rs;
-    h.out_ts = a.out_ts;
-    h.hdr = t.hdr;
-    h.mark = 1;
-    h.mark_pos = pos;
-    ProfScope ps(st, K_HASH_APPEND);
-    if (launch_hash_rows_tc(g, h, st) != cudaSuccess) return MP_ERR_CUDA;
-  } else {
-    ProfScope ps(st, K_HASH_APPEND);
-    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
-  }
-  if (g.match == MP_MATCH_SCAN) {
-    ProfScope ps(st, K_PLANES_APPEND);
-    if (launch_planes_append(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
-  }
-  if (g.nt == 0) {
-    ProfScope ps(st, K_MARK_APPENDED);
-    if (launch_mark_appended(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
-  }
-  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+  return a;
 }
 
-int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, const void* values,
-                        int32_t n, const void* q, float* out, void* scratch, size_t scratch_bytes,
-                        void* stream) {
-  int rc = check_config(cfg);
-  if (rc != MP_OK) return rc;
-  if (!tables || !keys || !values || !q || !out || !scratch) return MP_ERR_INVALID_ARG;
-  if (!aligned16(keys) || !aligned16(values) || !aligned16(q) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(tables) & 255u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
-    return MP_ERR_INVALID_ARG;
-  if (n < 1 || n > cfg->capacity) return MP_ERR_CAPACITY;
-  const Geometry g = geometry(cfg);
-  mp_decode_layout dl;
-  decode_layout(g, &dl);
-  if (scratch_bytes < dl.total_bytes) return MP_ERR_SCRATCH;
-  if (injected("decode")) return MP_ERR_INJECTED;
-  const TablesPtrs t = tables_ptrs(g, tables);
-  const DecodePtrs dp = decode_ptrs(g, scratch);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaGetLastError();
-  // 1. query codes (Algorithm 1 'Encode'): the query as it is, or (center_query) the
-  // query minus the center of its KV head, query head j of a sequence using KV head
-  // j / group
+static RowsHashTc append_rows_tc(const Geometry& g, const TablesPtrs& t, const void* keys, int pos) {
+  RowsHashTc h;
+  std::memset(&h, 0, sizeof(h));
+  h.x = static_cast<const __nv_bfloat16*>(keys) + int64_t(pos) * g.d;
+  h.x_rs = int64_t(g.cap) * g.d;
+  h.rows = g.batch * g.kvh;
+  h.groups = g.layers;
+  h.groups_per_w = 1;
+  h.wt16 = t.wt16;
+  h.negbeta = t.negbeta;
+  h.nb_div = 1;
+  h.out = t.codes + pos;
+  h.out_gs = int64_t(g.batch) * g.kvh * g.L * g.cap;
+  h.out_rs = int64_t(g.L) * g.cap;
+  h.out_ts = g.cap;
+  h.hdr = t.hdr;
+  h.mark = 1;
+  h.mark_pos = pos;
+  return h;
+}
+
+// Rows of a decode step's query hash (Algorithm 1 'Encode'): the query as it is, or
+// (center_query) the query minus the center of its KV head, query head j of a
+// sequence using KV head j / group.
+static HashRowsArgs query_rows_simt(const Geometry& g, const TablesPtrs& t, const void* q, const DecodePtrs& dp) {
   HashRowsArgs a;
   std::memset(&a, 0, sizeof(a));
   a.src = q;
@@ -519,32 +483,52 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
   a.out_gs = int64_t(g.batch) * g.qh * g.L;
   a.out_rs = g.L;
   a.out_ts = 1;
-  if (g.K == 0) {
-    if (cudaMemsetAsync(dp.qcodes, 0, size_t(g.queries) * g.L * sizeof(uint16_t), st) != cudaSuccess)
-      return MP_ERR_CUDA;
-  } else if (rows_on_tensor_cores(g, t)) {
-    RowsHashTc h;
-    std::memset(&h, 0, sizeof(h));
-    h.x = static_cast<const __nv_bfloat16*>(q);
-    h.x_rs = g.d;
-    h.rows = g.batch * g.qh;
-    h.groups = g.layers;
-    h.groups_per_w = 1;
-    h.wt16 = t.wt16;
-    h.negbeta = g.center_query ? t.negbeta : nullptr;
-    h.nb_div = g.group;
-    h.out = dp.qcodes;
-    h.out_gs = a.out_gs;
-    h.out_rs = a.out_rs;
-    h.out_ts = a.out_ts;
-    h.hdr = t.hdr;
-    ProfScope ps(st, K_HASH_QUERY);
-    if (launch_hash_rows_tc(g, h, st) != cudaSuccess) return MP_ERR_CUDA;
-  } else {
-    ProfScope ps(st, K_HASH_QUERY);
-    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  return a;
+}
+
+static RowsHashTc query_rows_tc(const Geometry& g, const TablesPtrs& t, const void* q, const DecodePtrs& dp) {
+  RowsHashTc h;
+  std::memset(&h, 0, sizeof(h));
+  h.x = static_cast<const __nv_bfloat16*>(q);
+  h.x_rs = g.d;
+  h.rows = g.batch * g.qh;
+  h.groups = g.layers;
+  h.groups_per_w = 1;
+  h.wt16 = t.wt16;
+  h.negbeta = g.center_query ? t.negbeta : nullptr;
+  h.nb_div = g.group;
+  h.out = dp.qcodes;
+  h.out_gs = int64_t(g.batch) * g.qh * g.L;
+  h.out_rs = g.L;
+  h.out_ts = 1;
+  h.hdr = t.hdr;
+  return h;
+}
+
+// After the appended key's codes are stored: its bit-planes (scan mode) and, with no
+// projections (K = 0), the appended end.
+static int finish_append(const Geometry& g, const TablesPtrs& t, int pos, cudaStream_t st) {
+  if (g.match == MP_MATCH_SCAN) {
+    ProfScope ps(st, K_PLANES_APPEND);
+    if (launch_planes_append(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
-  // 2. sampled set (Algorithm 1 'Query') + exact tokens
+  if (g.nt == 0) {
+    ProfScope ps(st, K_MARK_APPENDED);
+    if (launch_mark_appended(g, pos, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  return MP_OK;
+}
+
+// The query codes of K = 0 (every code is the empty code 0).
+static int zero_query_codes(const Geometry& g, const DecodePtrs& dp, cudaStream_t st) {
+  return cudaMemsetAsync(dp.qcodes, 0, size_t(g.queries) * g.L * sizeof(uint16_t), st) == cudaSuccess ? MP_OK
+                                                                                                     : MP_ERR_CUDA;
+}
+
+// Sampled sets (Algorithm 1 'Query') plus exact tokens, then the split-K
+// importance-weighted attention with its fused combine.
+static int match_and_attend(const Geometry& g, const TablesPtrs& t, const DecodePtrs& dp, int n, const void* keys,
+                            const void* values, const void* q, float* out, cudaStream_t st) {
   if (g.match == MP_MATCH_CSR) {
     ProfScope ps(st, K_MATCH_CSR);
     if (launch_match_csr(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
@@ -556,12 +540,111 @@ int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, co
     ProfScope ps(st, K_COMPACT);
     if (launch_compact(g, n, t, dp, st) != cudaSuccess) return MP_ERR_CUDA;
   }
-  // 3. split-K importance-weighted attention with fused combine
   const int splits = choose_splits(g, n);
-  {
-    ProfScope ps(st, K_ATTEND);
-    if (launch_attend(g, n, splits, t, keys, values, q, out, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+  ProfScope ps(st, K_ATTEND);
+  if (launch_attend(g, n, splits, t, keys, values, q, out, dp, st) != cudaSuccess) return MP_ERR_CUDA;
+  return MP_OK;
+}
+
+static int check_decode_args(const mp_config* cfg, void* tables, const void* keys, const void* values, int32_t n,
+                             const void* q, float* out, void* scratch, size_t scratch_bytes) {
+  if (!tables || !keys || !values || !q || !out || !scratch) return MP_ERR_INVALID_ARG;
+  if (!aligned16(keys) || !aligned16(values) || !aligned16(q) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(tables) & 255u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
+    return MP_ERR_INVALID_ARG;
+  if (n < 1 || n > cfg->capacity) return MP_ERR_CAPACITY;
+  mp_decode_layout dl;
+  decode_layout(geometry(cfg), &dl);
+  if (scratch_bytes < dl.total_bytes) return MP_ERR_SCRATCH;
+  return MP_OK;
+}
+
+}  // namespace mp
+
+extern "C" {
+
+int mp_append(const mp_config* cfg, void* tables, const void* keys, int32_t pos, void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (!keys || !tables) return MP_ERR_INVALID_ARG;
+  if (!aligned16(keys) || (reinterpret_cast<uintptr_t>(tables) & 255u)) return MP_ERR_INVALID_ARG;
+  if (pos < 0 || pos >= cfg->capacity) return MP_ERR_CAPACITY;
+  if (injected("append")) return MP_ERR_INJECTED;
+  const Geometry g = geometry(cfg);
+  const TablesPtrs t = tables_ptrs(g, tables);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  if (rows_on_tensor_cores(g, t)) {
+    const RowsHashTc h = append_rows_tc(g, t, keys, pos);
+    ProfScope ps(st, K_HASH_APPEND);
+    if (launch_hash_rows_tc(g, h, nullptr, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
+    const HashRowsArgs a = append_rows_simt(g, t, keys, pos);
+    ProfScope ps(st, K_HASH_APPEND);
+    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
   }
+  if ((rc = finish_append(g, t, pos, st)) != MP_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+int mp_decode_attention(const mp_config* cfg, void* tables, const void* keys, const void* values,
+                        int32_t n, const void* q, float* out, void* scratch, size_t scratch_bytes,
+                        void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if ((rc = check_decode_args(cfg, tables, keys, values, n, q, out, scratch, scratch_bytes)) != MP_OK) return rc;
+  if (injected("decode")) return MP_ERR_INJECTED;
+  const Geometry g = geometry(cfg);
+  const TablesPtrs t = tables_ptrs(g, tables);
+  const DecodePtrs dp = decode_ptrs(g, scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  if (g.K == 0) {
+    if ((rc = zero_query_codes(g, dp, st)) != MP_OK) return rc;
+  } else if (rows_on_tensor_cores(g, t)) {
+    const RowsHashTc h = query_rows_tc(g, t, q, dp);
+    ProfScope ps(st, K_HASH_QUERY);
+    if (launch_hash_rows_tc(g, h, nullptr, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
+    const HashRowsArgs a = query_rows_simt(g, t, q, dp);
+    ProfScope ps(st, K_HASH_QUERY);
+    if (launch_hash_rows(g, a, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  if ((rc = match_and_attend(g, t, dp, n, keys, values, q, out, st)) != MP_OK) return rc;
+  return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+int mp_decode_step(const mp_config* cfg, void* tables, const void* keys, const void* values, int32_t pos,
+                   const void* q, float* out, void* scratch, size_t scratch_bytes, void* stream) {
+  int rc = check_config(cfg);
+  if (rc != MP_OK) return rc;
+  if (pos < 0 || pos >= cfg->capacity) return MP_ERR_CAPACITY;
+  if ((rc = check_decode_args(cfg, tables, keys, values, pos + 1, q, out, scratch, scratch_bytes)) != MP_OK)
+    return rc;
+  if (injected("append") || injected("decode")) return MP_ERR_INJECTED;
+  const Geometry g = geometry(cfg);
+  const TablesPtrs t = tables_ptrs(g, tables);
+  const DecodePtrs dp = decode_ptrs(g, scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  // the appended keys and the queries of the step, hashed by one launch (the appended
+  // codes are stored before the match kernel reads them: stream order)
+  if (g.K == 0) {
+    if ((rc = zero_query_codes(g, dp, st)) != MP_OK) return rc;
+  } else if (rows_on_tensor_cores(g, t)) {
+    const RowsHashTc ha = append_rows_tc(g, t, keys, pos);
+    const RowsHashTc hq = query_rows_tc(g, t, q, dp);
+    ProfScope ps(st, K_HASH_STEP);
+    if (launch_hash_rows_tc(g, ha, &hq, st) != cudaSuccess) return MP_ERR_CUDA;
+  } else {
+    const HashRowsArgs aa = append_rows_simt(g, t, keys, pos);
+    const HashRowsArgs aq = query_rows_simt(g, t, q, dp);
+    ProfScope ps(st, K_HASH_STEP);
+    if (launch_hash_rows(g, aa, st) != cudaSuccess || launch_hash_rows(g, aq, st) != cudaSuccess)
+      return MP_ERR_CUDA;
+  }
+  if ((rc = finish_append(g, t, pos, st)) != MP_OK) return rc;
+  if ((rc = match_and_attend(g, t, dp, pos + 1, keys, values, q, out, st)) != MP_OK) return rc;
   return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 

@@ -398,10 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // cores, with the roles of the operands swapped: A = 256 W columns (two M = 128
 // halves), B = up to 256 rows (N), so that a tensor-memory lane is a W column and a
 // ballot across a warp's lanes gives one row's sign bits of 32 columns at once.
-// One CTA per (W group, 256-column tile, row block): thread 0 issues the TMA loads and
-// the MMAs, then all 8 warps read the accumulator (warp w: half w / 4, lanes of
-// quarter w % 4), add -beta for appended keys, ballot the signs into a shared
-// [row][32-column block] bitmap, and cut the codes.
+// One launch hashes one or two row sets (a decode step's appended keys and its
+// queries): per W group the sets are laid end to end, each rounded up to 32 rows, and
+// row blocks of up to 256 of these rows share one load of a W tile. One CTA per (W
+// group, 256-column tile, row block): thread 0 issues the TMA loads (the rows in boxes
+// of 32, each from its set's tensor map) and the MMAs, then all 8 warps read the
+// accumulator (warp w: half w / 4, lanes of quarter w % 4), add -beta where the set is
+// centered, ballot the signs into a shared [row][32-column block] bitmap, and cut the
+// codes.
 // ---------------------------------------------------------------------------------
 constexpr int kRowsWarps = 8;
 
@@ -418,17 +422,24 @@ struct RowsLayout {
   __host__ __device__ static constexpr uint32_t bytes(int nr) { return ctl_off(nr) + 64u; }  // 3 barriers + slots
 };
 
-struct RowsTcArgs {
-  int rows;          // rows per group
-  int nr;            // rows per CTA (multiple of 32, <= 256)
-  int groups_per_w;  // group g uses W matrix g / groups_per_w
-  int w_rows;        // W rows between consecutive W matrices (0: shared)
+// One set of rows hashed by k_hash_rows_tc.
+struct RowSetTc {
+  int rows;              // rows per group
+  int nr32;              // rows rounded up to a multiple of 32
   const float* negbeta;  // -beta [U][kltc] added to row r of group g: unit (g * rows + r) / nb_div
                          // (nullptr: rows hashed as they are)
   int nb_div;
-  int kltc;
   uint16_t* out;
   int64_t out_gs, out_rs, out_ts;
+};
+
+struct RowsTcArgs {
+  RowSetTc set[2];   // set[1].rows = 0 when one set is hashed
+  int vrows;         // set[0].nr32 + set[1].nr32
+  int nr;            // rows per CTA (multiple of 32, <= 256)
+  int groups_per_w;  // group g uses W matrix g / groups_per_w
+  int w_rows;        // W rows between consecutive W matrices (0: shared)
+  int kltc;
   DevHeader* hdr;    // status word
   int mark;          // appends: raise the appended end to mark_pos + 1
   int mark_pos;
@@ -436,8 +447,8 @@ struct RowsTcArgs {
 
 template <int D>
 __global__ void __launch_bounds__(kRowsWarps * 32)
-    k_hash_rows_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, RowsTcArgs a,
-                   int L, int K, int tpt) {
+    k_hash_rows_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX0,
+                   const __grid_constant__ CUtensorMap tmX1, const RowsTcArgs a, int L, int K, int tpt) {
   using Lay = RowsLayout<D>;
   constexpr int kSub = Lay::kSub;
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -452,10 +463,12 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   volatile uint32_t* abort = tmem_slot + 1;
   const int g = blockIdx.z, n = blockIdx.y, rb = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = rb * nr;                   // first row of this CTA within its group
-  const int nvalid = min(nr, a.rows - r0);  // rows stored
+  const int v0 = rb * nr;                  // first row of this CTA in the group's row list
+  const int nrow = min(nr, a.vrows - v0);  // rows of this CTA (multiple of 32)
   uint32_t ncols = 32;
-  while (ncols < uint32_t(2 * nr)) ncols <<= 1;
+  while (ncols < uint32_t(2 * nrow)) ncols <<= 1;
+  // row v of the group's list belongs to set 1 from set[0].nr32 on
+  const int split = a.set[0].nr32;
 
   if (threadIdx.x == 0) {
     mbar_init(full, 1);
@@ -468,7 +481,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
       else atomicMax(&a.hdr->appended_end, a.mark_pos + 1);
     }
   }
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) bits[i * 9 + 8] = 0u;
+  for (int i = threadIdx.x; i < nrow; i += blockDim.x) bits[i * 9 + 8] = 0u;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
                  "r"(ncols)
@@ -485,16 +498,20 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
     // buffer in turn; the rows are loaded with the first term
     const int terms = a.hdr->w_terms3 ? 3 : 1;
     const int wrow = (g / a.groups_per_w) * a.w_rows + n * 256;
-    const int xrow = g * a.rows + r0;
-    // D[col][row]: M = 128 W columns per half, N = nr rows
+    // D[col][row]: M = 128 W columns per half, N = nrow rows
     const uint32_t idesc =
-        (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nr >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+        (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(nrow >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     for (int j = 0; j < terms; ++j) {
       if (j > 0 && !mbar_wait(mdone, (j - 1) & 1, abort)) break;
-      mbar_expect_tx(full, uint32_t(kSub) * (Lay::kABytes + (j == 0 ? uint32_t(nr) * 128u : 0u)));
+      mbar_expect_tx(full, uint32_t(kSub) * (Lay::kABytes + (j == 0 ? uint32_t(nrow) * 128u : 0u)));
       for (int s = 0; s < kSub; ++s) {
         tma_load_2d(sm + Lay::a_off(s), &tmW, s * 64, wrow + j * a.kltc, full);
-        if (j == 0) tma_load_2d(sm + Lay::b_off(s, nr), &tmX, s * 64, xrow, full);
+        if (j == 0)
+          for (int b = 0; b < nrow / 32; ++b) {
+            const int v = v0 + 32 * b, st = v >= split ? 1 : 0;
+            const int xrow = g * a.set[st].rows + v - (st ? split : 0);
+            tma_load_2d(sm + Lay::b_off(s, nr) + uint32_t(b) * 4096u, st ? &tmX1 : &tmX0, s * 64, xrow, full);
+          }
       }
       if (!mbar_wait(full, j & 1, abort)) break;
       fence_after();
@@ -505,29 +522,32 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
           const int s = kk >> 2, off = (kk & 3) * 32;
           const uint64_t da = sw128_desc(saddr(sm + Lay::a_off(s)) + uint32_t(h) * 16384u + off);
           const uint64_t db = sw128_desc(saddr(sm + Lay::b_off(s, nr)) + off);
-          mma_bf16(tmem + uint32_t(h * nr), da, db, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tmem + uint32_t(h * nrow), da, db, idesc, (j > 0 || kk > 0) ? 1u : 0u);
         }
       mma_commit(j + 1 < terms ? mdone : accb);
     }
   }
   __syncwarp();
-  // epilogue: all warps. -beta of the first 32 rows is fetched before the wait for the
-  // accumulator (it does not depend on it). Row j of chunk ch is row r0 + 32 ch + j of
-  // group g, centered with unit (g * rows + r0 + 32 ch + j) / nb_div, walked as a
-  // quotient and remainder so that no division runs per row.
+  // epilogue: all warps. Each 32-row chunk lies in one set. Row j of chunk ch is row
+  // local + j of its set, centered (if the set is) with unit (g * rows + local + j) /
+  // nb_div, walked as a quotient and remainder so that no division runs per row; the
+  // -beta of the first chunk is fetched before the wait for the accumulator.
   const int h = warp >> 2, quarter = warp & 3;
   const int col = h * 128 + quarter * 32 + lane;  // column within the 256-column tile
-  const float* nbc = a.negbeta ? a.negbeta + int64_t(n) * 256 + col : nullptr;
-  const int row_base = g * a.rows + r0;
-  int nb_unit = row_base / a.nb_div, nb_rem = row_base - nb_unit * a.nb_div;
   float nb[32];
   auto fetch_nb = [&](int ch) {
+    const int v = v0 + 32 * ch, st = v >= split ? 1 : 0;
+    const RowSetTc& S = a.set[st];
+    const int local = v - (st ? split : 0);
+    const float* nbc = S.negbeta ? S.negbeta + int64_t(n) * 256 + col : nullptr;
+    const int row_base = g * S.rows + local;
+    int unit = row_base / S.nb_div, rem = row_base - unit * S.nb_div;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      nb[j] = (nbc && ch * 32 + j < nvalid) ? __ldg(nbc + int64_t(nb_unit) * a.kltc) : 0.f;
-      if (++nb_rem == a.nb_div) {
-        nb_rem = 0;
-        ++nb_unit;
+      nb[j] = (nbc && local + j < S.rows) ? __ldg(nbc + int64_t(unit) * a.kltc) : 0.f;
+      if (++rem == S.nb_div) {
+        rem = 0;
+        ++unit;
       }
     }
   };
@@ -535,10 +555,10 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   const bool ok = __all_sync(0xffffffffu, mbar_wait(accb, 0, abort));
   if (ok) {
     fence_after();
-    for (int ch = 0; ch < (nvalid + 31) / 32; ++ch) {
+    for (int ch = 0; ch < nrow / 32; ++ch) {
       if (ch > 0) fetch_nb(ch);
       uint32_t r[32];
-      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * nr + ch * 32), r);
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * nrow + ch * 32), r);
       tmem_wait_ld();
       uint32_t mine = 0;
 #pragma unroll
@@ -546,8 +566,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
         const uint32_t w = __ballot_sync(0xffffffffu, __uint_as_float(r[j]) + nb[j] > 0.f);
         if (lane == j) mine = w;
       }
-      const int row = ch * 32 + lane;
-      if (row < nr) bits[row * 9 + h * 4 + quarter] = mine;
+      bits[(ch * 32 + lane) * 9 + h * 4 + quarter] = mine;
     }
   }
   fence_before();
@@ -561,14 +580,17 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
     return;
   }
   const uint32_t mask = (1u << K) - 1u;
-  for (int i = threadIdx.x; i < nvalid * tpt; i += blockDim.x) {
+  for (int i = threadIdx.x; i < nrow * tpt; i += blockDim.x) {
     const int row = i / tpt, tl = i - row * tpt;
     const int t = n * tpt + tl;
-    if (t >= L) continue;
+    const int v = v0 + row, st = v >= split ? 1 : 0;
+    const RowSetTc& S = a.set[st];
+    const int local = v - (st ? split : 0);
+    if (t >= L || local >= S.rows) continue;
     const int c0 = tl * K;
-    const uint64_t v = uint64_t(bits[row * 9 + (c0 >> 5)]) | (uint64_t(bits[row * 9 + (c0 >> 5) + 1]) << 32);
-    a.out[int64_t(g) * a.out_gs + int64_t(r0 + row) * a.out_rs + int64_t(t) * a.out_ts] =
-        uint16_t(uint32_t(v >> (c0 & 31)) & mask);
+    const uint64_t w = uint64_t(bits[row * 9 + (c0 >> 5)]) | (uint64_t(bits[row * 9 + (c0 >> 5) + 1]) << 32);
+    S.out[int64_t(g) * S.out_gs + int64_t(local) * S.out_rs + int64_t(t) * S.out_ts] =
+        uint16_t(uint32_t(w >> (c0 & 31)) & mask);
   }
 }
 
@@ -632,41 +654,65 @@ cudaError_t launch_tc(const Geometry& g, const void* keys, int n_prefill, const 
   return cudaGetLastError();
 }
 
+static RowSetTc row_set(const RowsHashTc& h) {
+  RowSetTc r;
+  r.rows = h.rows;
+  r.nr32 = (h.rows + 31) / 32 * 32;
+  r.negbeta = h.negbeta;
+  r.nb_div = h.nb_div > 0 ? h.nb_div : 1;
+  r.out = h.out;
+  r.out_gs = h.out_gs;
+  r.out_rs = h.out_rs;
+  r.out_ts = h.out_ts;
+  return r;
+}
+
 template <int D>
-cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st) {
+cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h0, const RowsHashTc* h1, cudaStream_t st) {
   RowsTcArgs a;
-  a.rows = h.rows;
-  a.nr = std::min(256, (h.rows + 31) / 32 * 32);
-  a.groups_per_w = h.groups_per_w;
+  a.set[0] = row_set(h0);
+  if (h1) {
+    a.set[1] = row_set(*h1);
+  } else {
+    a.set[1] = a.set[0];
+    a.set[1].rows = 0;
+    a.set[1].nr32 = 0;
+  }
+  a.vrows = a.set[0].nr32 + a.set[1].nr32;
+  a.nr = std::min(256, a.vrows);
+  a.groups_per_w = h0.groups_per_w;
   a.w_rows = g.w_per_layer ? 3 * g.kltc : 0;
-  a.negbeta = h.negbeta;
-  a.nb_div = h.nb_div > 0 ? h.nb_div : 1;
   a.kltc = g.kltc;
-  a.out = h.out;
-  a.out_gs = h.out_gs;
-  a.out_rs = h.out_rs;
-  a.out_ts = h.out_ts;
-  a.hdr = h.hdr;
-  a.mark = h.mark;
-  a.mark_pos = h.mark_pos;
-  CUtensorMap mw, mx;
-  if (!make_map(&mw, h.wt16, uint64_t(g.d), uint64_t(g.n_w) * 3 * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_strided(&mx, h.x, uint64_t(g.d), uint64_t(h.rows) * h.groups, uint64_t(h.x_rs) * 2, 64,
-                        uint32_t(a.nr), CU_TENSOR_MAP_SWIZZLE_128B))
+  a.hdr = h0.hdr;
+  a.mark = h0.mark || (h1 && h1->mark);
+  a.mark_pos = h0.mark ? h0.mark_pos : (h1 ? h1->mark_pos : 0);
+  CUtensorMap mw, mx0, mx1;
+  if (!make_map(&mw, h0.wt16, uint64_t(g.d), uint64_t(g.n_w) * 3 * g.kltc, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_strided(&mx0, h0.x, uint64_t(g.d), uint64_t(h0.rows) * h0.groups, uint64_t(h0.x_rs) * 2, 64, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (h1) {
+    if (!make_map_strided(&mx1, h1->x, uint64_t(g.d), uint64_t(h1->rows) * h1->groups, uint64_t(h1->x_rs) * 2, 64,
+                          32, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else {
+    mx1 = mx0;
+  }
   const size_t smem = RowsLayout<D>::bytes(a.nr) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_hash_rows_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid((h.rows + a.nr - 1) / a.nr, g.nt, h.groups);
-  k_hash_rows_tc<D><<<grid, kRowsWarps * 32, smem, st>>>(mw, mx, a, g.L, g.K, g.tpt);
+  dim3 grid((a.vrows + a.nr - 1) / a.nr, g.nt, h0.groups);
+  k_hash_rows_tc<D><<<grid, kRowsWarps * 32, smem, st>>>(mw, mx0, mx1, a, g.L, g.K, g.tpt);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st) {
-  if (h.rows <= 0 || h.groups <= 0 || g.nt == 0) return cudaSuccess;
-  return g.d == 128 ? launch_rows_tc<128>(g, h, st) : launch_rows_tc<64>(g, h, st);
+cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h0, const RowsHashTc* h1, cudaStream_t st) {
+  if (h1 && h1->rows <= 0) h1 = nullptr;
+  if (h0.rows <= 0 || h0.groups <= 0 || g.nt == 0) return cudaSuccess;
+  if (h1 && (h1->groups != h0.groups || h1->groups_per_w != h0.groups_per_w)) return cudaErrorInvalidValue;
+  return g.d == 128 ? launch_rows_tc<128>(g, h0, h1, st) : launch_rows_tc<64>(g, h0, h1, st);
 }
 
 cudaError_t launch_hash_keys_tc(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,

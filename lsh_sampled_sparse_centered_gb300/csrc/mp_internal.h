@@ -117,7 +117,7 @@ struct RowsHashTc {
 };
 
 // ---- launchers (each returns cudaError_t of the launch) ----
-cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h, cudaStream_t st);
+cudaError_t launch_hash_rows_tc(const Geometry& g, const RowsHashTc& h0, const RowsHashTc* h1, cudaStream_t st);
 cudaError_t launch_prepare_w(const Geometry& g, const float* W, const TablesPtrs& t, cudaStream_t st);
 cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, const TablesPtrs& t,
                           cudaStream_t st);

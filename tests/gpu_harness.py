@@ -50,6 +50,12 @@ class DeviceRun:
                                     self.scratch)
         return self.out
 
+    def step(self, step: int, n: int):
+        """Append token n - 1 and decode over n tokens in one call (mp_decode_step)."""
+        q = self.queries[step].contiguous()
+        self.mp.mp_decode_step(self.cfg, self.tables, self.keys, self.values, n - 1, q, self.out, self.scratch)
+        return self.out
+
     def status(self) -> int:
         return self.mp.mp_get_status(self.tables)
 
@@ -188,11 +194,13 @@ def check_planes(planes: np.ndarray, codes: np.ndarray, n: int, K: int) -> None:
 
 def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshold: int = 2,
                    units=None, qheads=None, steps=None, check_csr_tables: int = 8, tol: float = 2e-3,
-                   match_mode: int = 0, centering: bool = True, center_query: bool = False) -> dict:
+                   match_mode: int = 0, centering: bool = True, center_query: bool = False,
+                   use_step: bool = False) -> dict:
     """Build, append and decode `wl` through the C ABI and compare every stage with the
     oracle on the chosen units / query heads / steps. With center_query the query is
     hashed as q - c and p is the collision probability of q - c with k - c (the oracle's
-    other reading). Returns counters for reporting."""
+    other reading). With use_step (appending workloads) every step is one mp_decode_step
+    call instead of mp_append + mp_decode_attention. Returns counters for reporting."""
     run = DeviceRun(mp, wl, tensors, device, threshold, match_mode, centering, center_query)
     run.build()
     torch.cuda.synchronize()
@@ -234,9 +242,12 @@ def check_workload(mp, wl: WL.Workload, tensors: dict, device="cuda:0", threshol
     last = max(steps) if steps else -1
     for step in range(last + 1):
         n = wl.seq_len(step)
-        if wl.append:
-            run.append(n - 1)
-        out_t = run.decode(step, n)
+        if wl.append and use_step:
+            out_t = run.step(step, n)
+        else:
+            if wl.append:
+                run.append(n - 1)
+            out_t = run.decode(step, n)
         if step not in steps:
             continue
         out = out_t.cpu().numpy()

@@ -115,6 +115,15 @@ def test_argument_errors_return_before_any_launch(mp):
                        ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_CAPACITY
     assert mp.call_raw("mp_decode_attention", ctypes.byref(c), fake, fake, None, 100, fake, fake, fake,
                        ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_INVALID_ARG
+    # the decode step: the appended position bounds the capacity, the scratch size as above
+    assert mp.call_raw("mp_decode_step", ctypes.byref(c), fake, fake, fake, 4096, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_decode_step", ctypes.byref(c), fake, fake, fake, -1, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_CAPACITY
+    assert mp.call_raw("mp_decode_step", ctypes.byref(c), fake, fake, fake, 100, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes - 1), None) == mp.MP_ERR_SCRATCH
+    assert mp.call_raw("mp_decode_step", ctypes.byref(c), fake, fake, fake, 100, fake, None, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_INVALID_ARG
     assert mp.call_raw("mp_get_status", None, None, None) == mp.MP_ERR_INVALID_ARG
     assert mp.mp_status_string(mp.MP_ERR_SCRATCH) == "scratch buffer too small"
 
@@ -129,6 +138,8 @@ def test_fault_injection_on_the_host(mp, monkeypatch):
     monkeypatch.setenv("MP_FAULT_INJECT", "all")
     assert mp.call_raw("mp_build_tables", ctypes.byref(c), fake, 10, fake, fake, None) == mp.MP_ERR_INJECTED
     assert mp.call_raw("mp_append", ctypes.byref(c), fake, fake, 20, None) == mp.MP_ERR_INJECTED
+    assert mp.call_raw("mp_decode_step", ctypes.byref(c), fake, fake, fake, 100, fake, fake, fake,
+                       ctypes.c_size_t(dl.total_bytes), None) == mp.MP_ERR_INJECTED
     with pytest.raises(mp.MagicPigError) as e:
         mp.mp_append(c, fake, fake, 20, stream=0)
     assert e.value.code == mp.MP_ERR_INJECTED

@@ -215,3 +215,61 @@ def test_scan_match_mode(mp, wl):
                          check_csr_tables=wl.L)
     _report(f"scan {wl.name}", rep)
     assert rep["match_mode"] == mp.MP_MATCH_SCAN
+
+
+# ----------------------------------------------------------------------------------
+# mp_decode_step: the append and the decode of a step in one call, the appended keys
+# and the queries hashed by one launch
+# ----------------------------------------------------------------------------------
+
+STEP_CASES = {
+    "gqa4": WL.WORKLOADS[1].replace(n_prefill=5000, steps=20, append=True, window=8),
+    "gqa8-b4": WL.WORKLOADS[4].replace(n_prefill=4000, steps=12, window=8),       # two row blocks per layer
+    "mha-b16": WL.WORKLOADS[3].replace(n_prefill=3000, steps=3, window=8),        # five row blocks per layer
+    "ragged": RAGGED,
+}
+
+
+@pytest.mark.parametrize("case,path,kw", [
+    ("gqa4", "tc", {}), ("gqa4", "simt", {}), ("gqa4", "tc", dict(center_query=True)),
+    ("gqa8-b4", "tc", {}), ("gqa8-b4", "tc", dict(center_query=True)), ("mha-b16", "tc", {}),
+    ("ragged", "tc", {}), ("ragged", "tc", dict(w_bf16=False)), ("ragged", "tc", dict(match_mode=2)),
+    ("gqa4", "tc", dict(K=0, L=3)),
+])
+def test_decode_step_equals_append_then_decode(mp, monkeypatch, case, path, kw):
+    """Same codes, query codes, lists and outputs, bit for bit, as the two separate calls."""
+    monkeypatch.setenv("MP_HASH_PATH", path)
+    kw = dict(kw)
+    cq = kw.pop("center_query", False)
+    mode = kw.pop("match_mode", 0)
+    wl = STEP_CASES[case].replace(**kw)
+    t = WL.generate(wl)
+    a = DeviceRun(mp, wl, t, "cuda:0", match_mode=mode, center_query=cq)
+    b = DeviceRun(mp, wl, t, "cuda:0", match_mode=mode, center_query=cq)
+    a.build()
+    b.build()
+    for step in range(wl.steps):
+        n = wl.seq_len(step)
+        a.append(n - 1)
+        oa = a.decode(step, n).clone()
+        ob = b.step(step, n).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), (case, step)
+        qa, la, sa = a.decode_state()
+        qb, lb, sb = b.decode_state()
+        np.testing.assert_array_equal(qa, qb)
+        np.testing.assert_array_equal(la, lb)
+        np.testing.assert_array_equal(sa, sb)
+        if step in (0, wl.steps - 1):
+            for qi in range(len(la)):
+                np.testing.assert_array_equal(a.list_of(qi, int(la[qi])), b.list_of(qi, int(lb[qi])))
+    assert (a.status() & ~mp.MP_STATUS_W_NOT_BF16) == 0 and (b.status() & ~mp.MP_STATUS_W_NOT_BF16) == 0
+    np.testing.assert_array_equal(a.codes(), b.codes())
+
+
+@pytest.mark.parametrize("case,kw", [("ragged", {}), ("gqa8-b4", dict(center_query=True))])
+def test_decode_step_against_the_oracle(mp, case, kw):
+    wl = STEP_CASES[case]
+    steps = [0, 15, 16, 17, 39] if case == "ragged" else [0, 11]
+    rep = check_workload(mp, wl, WL.generate(wl), steps=steps, check_csr_tables=wl.L, use_step=True, **kw)
+    _report(f"decode step {case}", rep)
