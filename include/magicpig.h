@@ -71,6 +71,10 @@ extern "C" {
 #define MP_STATUS_WAIT_TIMEOUT 0x2u /* a bounded wait on an mbarrier gave up */
 #define MP_STATUS_APPEND_GAP 0x4u   /* decode needed codes of a token never appended */
 #define MP_STATUS_NOT_BUILT 0x8u    /* decode or append on tables that were never built */
+#define MP_STATUS_BAD_INDEX 0x10u   /* bounds-checking build only (compiled with MP_CHECK=1): a
+                                       kernel met an index outside its buffer (a code of 2^K or
+                                       more, a bucket run past its segment, a list entry past the
+                                       capacity) and skipped that access */
 
 /* element types */
 #define MP_DTYPE_F32 0

@@ -13,7 +13,10 @@ import os
 from typing import Optional, Union
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libmagicpig.so")
+# MP_BOUNDS_CHECK=1 loads the bounds-checking build (kernels test data-derived indices
+# and set MP_STATUS_BAD_INDEX instead of touching memory outside their buffers)
+BOUNDS_CHECK = os.environ.get("MP_BOUNDS_CHECK") == "1"
+LIB_PATH = os.path.join(_PKG, "_lib", "libmagicpig_check.so" if BOUNDS_CHECK else "libmagicpig.so")
 
 MP_OK = 0
 MP_ERR_INVALID_ARG = -1
@@ -27,6 +30,7 @@ MP_STATUS_W_NOT_BF16 = 0x1
 MP_STATUS_WAIT_TIMEOUT = 0x2
 MP_STATUS_APPEND_GAP = 0x4
 MP_STATUS_NOT_BUILT = 0x8
+MP_STATUS_BAD_INDEX = 0x10
 
 MP_DTYPE_F32 = 0
 MP_DTYPE_BF16 = 1
@@ -37,8 +41,8 @@ MP_MATCH_SCAN = 2
 EXACT_FLAG = 0x80000000
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libmagicpig.so is not built ({LIB_PATH}); run "
-                      "`python lsh_sampled_sparse_centered_gb300/build.py`")
+    raise ImportError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
+                      "`python lsh_sampled_sparse_centered_gb300/build.py`" + (" --check" if BOUNDS_CHECK else ""))
 _lib = ctypes.CDLL(LIB_PATH)
 
 

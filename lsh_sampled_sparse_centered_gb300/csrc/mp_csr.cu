@@ -26,7 +26,8 @@ __device__ __forceinline__ uint32_t code_of(const uint4& v, int e) {
 
 __global__ void __launch_bounds__(kCsrThreads, 2) k_csr_build(const uint16_t* __restrict__ codes,
                                                            uint16_t* __restrict__ off, uint16_t* __restrict__ ids,
-                                                           int cap, int nb, int nseg, int lo, int hi) {
+                                                           int cap, int nb, int nseg, int lo, int hi,
+                                                           uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int64_t table = blockIdx.x;  // unit * L + t
   const int s = blockIdx.y;
@@ -54,7 +55,8 @@ __global__ void __launch_bounds__(kCsrThreads, 2) k_csr_build(const uint16_t* __
     const int i0 = ch * 8 - skip;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      if (unsigned(i0 + e) < unsigned(m)) atomicAdd(&cursor[code_of(v, e)], 1u);
+      if (unsigned(i0 + e) < unsigned(m) && in_range(code_of(v, e) < uint32_t(nb), status))
+        atomicAdd(&cursor[code_of(v, e)], 1u);
   }
   __syncthreads();
 
@@ -101,7 +103,8 @@ __global__ void __launch_bounds__(kCsrThreads, 2) k_csr_build(const uint16_t* __
     const int i0 = ch * 8 - skip;
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      if (unsigned(i0 + e) < unsigned(m)) sorted[atomicAdd(&cursor[code_of(v, e)], 1u)] = uint16_t(i0 + e);
+      if (unsigned(i0 + e) < unsigned(m) && in_range(code_of(v, e) < uint32_t(nb), status))
+        sorted[atomicAdd(&cursor[code_of(v, e)], 1u)] = uint16_t(i0 + e);
   }
   __syncthreads();
   // out: whole 16-byte chunks inside the segment as one store, the ragged ends by element
@@ -126,7 +129,7 @@ cudaError_t launch_csr_build(const Geometry& g, int n_prefill, const TablesPtrs&
   const size_t smem = ((size_t(g.nb) * 4 + 15) & ~size_t(15)) + size_t(kCsrSeg + 16) * 2;
   cudaFuncSetAttribute(k_csr_build, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   dim3 grid(g.units * g.L, segs);
-  k_csr_build<<<grid, kCsrThreads, smem, st>>>(t.codes, t.off, t.ids, g.cap, g.nb, g.nseg, lo, hi);
+  k_csr_build<<<grid, kCsrThreads, smem, st>>>(t.codes, t.off, t.ids, g.cap, g.nb, g.nseg, lo, hi, &t.hdr->status);
   return cudaGetLastError();
 }
 

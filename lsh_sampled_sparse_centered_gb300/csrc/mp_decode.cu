@@ -22,7 +22,7 @@ namespace mp {
 // [n_sink, n - window); with threshold 1 it is seen1. Compaction writes S in
 // ascending token order, then the exact tokens (bit 31 set).
 constexpr int kMatchWarps = 8;
-constexpr int kChunkUnroll = 3;  // 16-byte chunks of ids in flight per thread
+constexpr int kChunkUnroll = 4;  // 16-byte chunks of ids in flight per thread
 
 // Exclusive scan of v[0..n) in place by the whole block; v[n] receives the total.
 __device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {
@@ -56,7 +56,7 @@ __device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hdr,
+__global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
                                                    const uint16_t* __restrict__ off,
@@ -93,37 +93,40 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
   }
   for (int i = threadIdx.x; i < (body >> 2); i += blockDim.x) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0u, 0u, 0u, 0u);
   for (int i = (body & ~3) + threadIdx.x; i < body; i += blockDim.x) sm[i] = 0u;
-  // Tokens hashed at build time: the query's bucket in every (table, segment), one run
-  // of ids each. Thread t < L reads the query's code of table t and the bucket's start
-  // and end in every segment. Every run is covered by the 16-byte chunks that hold it;
-  // the chunks of all runs of the head are numbered consecutively (a block scan of the
-  // per-run chunk counts) and split evenly over the threads, so each thread has about
-  // the same number of chunks, reads them kChunkUnroll at a time (all loads in flight
-  // before their marks) and marks every id of a chunk itself.
-  const int64_t tbase = int64_t(unit) * L;
-  const int lo_b = min(s, n0);  // first token bucketed at build time
-  const int nsu = (built && n0 > lo_b) ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
-  const int runs = L * nsu;
-  const uintptr_t idb = reinterpret_cast<uintptr_t>(ids + tbase * cap);  // the unit's id arrays
-  const uintptr_t idb16 = idb & ~uintptr_t(15);
-  // run r = t * nsu + sg: {first chunk (16-byte units from idb16), size | skip << 16 | sg << 19},
-  // skip = ids of the first chunk before the run; pre[r] = chunks of runs before r
-  for (int t = threadIdx.x; t < L; t += blockDim.x) {
-    const uint32_t code = qcodes[int64_t(qh) * L + t];
-    qc[t] = uint16_t(code);
-    const uint16_t* o = off + (tbase + t) * int64_t(nb + 1) * nseg + int64_t(code) * nseg;
-    for (int sg = 0; sg < nsu; ++sg) {
-      const uint32_t b0 = __ldg(o + sg), b1 = __ldg(o + nseg + sg);
-      const uint32_t sz = b1 - b0;
-      const uintptr_t a = idb + 2u * (uint64_t(t) * uint64_t(cap) + uint64_t(sg) * kCsrSeg + b0);
-      const uint32_t c0 = uint32_t((a - idb16) >> 4);
-      bkt[t * nsu + sg] = make_uint2(c0, sz | (uint32_t((a & 15u) >> 1) << 16) | (uint32_t(sg) << 19));
-      pre[t * nsu + sg] = sz ? uint32_t(((a + 2u * sz - 1u) >> 4) - (a >> 4) + 1u) : 0u;
-    }
-  }
+  for (int t = threadIdx.x; t < L; t += blockDim.x) qc[t] = qcodes[int64_t(qh) * L + t];
   __syncthreads();
 
   if (built && hi > lo) {
+    // Tokens hashed at build time: the query's bucket in every (table, segment), one run
+    // of ids each. Every run is covered by the 16-byte chunks that hold it; the chunks of
+    // all runs of the head are numbered consecutively (a block scan of the per-run chunk
+    // counts) and split evenly over the threads, so each thread has about the same number
+    // of chunks, reads them kChunkUnroll at a time (all loads in flight before their
+    // marks) and marks every id of a chunk itself.
+    const int64_t tbase = int64_t(unit) * L;
+    const int lo_b = min(s, n0);  // first token bucketed at build time
+    const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
+    const int runs = L * nsu;
+    const uintptr_t idb = reinterpret_cast<uintptr_t>(ids + tbase * cap);  // the unit's id arrays
+    const uintptr_t idb16 = idb & ~uintptr_t(15);
+    // run r = t * nsu + sg: {first chunk (16-byte units from idb16), size | skip << 16 | sg << 19},
+    // skip = ids of the first chunk before the run; pre[r] = chunks of runs before r
+    for (int t = threadIdx.x; t < L; t += blockDim.x) {
+      const bool code_ok = in_range(qc[t] < uint32_t(nb), &hdr->status);
+      const uint16_t* o = off + (tbase + t) * int64_t(nb + 1) * nseg + int64_t(code_ok ? qc[t] : 0) * nseg;
+      for (int sg = 0; sg < nsu; ++sg) {
+        const uint32_t b0 = __ldg(o + sg), b1 = __ldg(o + nseg + sg);
+        // a run lies inside its segment (whose tokens number min(32768, n0 - lo_b - 32768 sg))
+        const bool run_ok = code_ok && in_range(b0 <= b1 && int(b1) <= min(kCsrSeg, n0 - lo_b - sg * kCsrSeg),
+                                                &hdr->status);
+        const uint32_t sz = run_ok ? b1 - b0 : 0u;
+        const uintptr_t a = idb + 2u * (uint64_t(t) * uint64_t(cap) + uint64_t(sg) * kCsrSeg + b0);
+        const uint32_t c0 = uint32_t((a - idb16) >> 4);
+        bkt[t * nsu + sg] = make_uint2(c0, sz | (uint32_t((a & 15u) >> 1) << 16) | (uint32_t(sg) << 19));
+        pre[t * nsu + sg] = sz ? uint32_t(((a + 2u * sz - 1u) >> 4) - (a >> 4) + 1u) : 0u;
+      }
+    }
+    __syncthreads();
     block_exclusive_scan(pre, runs);  // pre[runs] = total chunks
     const uint32_t total = pre[runs];
     const uint32_t cb = uint32_t((uint64_t(total) * threadIdx.x) / blockDim.x);
@@ -138,16 +141,13 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
       }
       const uint4* cbase = reinterpret_cast<const uint4*>(idb16);
       for (uint32_t c = cb; c < ce; c += kChunkUnroll) {
-        // per chunk: the loaded ids, the token of its segment's first id, and `vm`: bit q
-        // set if id slot q lies in the run, bits 8.. the bound below which an id is in
-        // the LSH region (hi - the segment's first token, at most 65535)
         uint4 v[kChunkUnroll];
-        uint32_t tb[kChunkUnroll], vm[kChunkUnroll];
+        uint32_t tok0[kChunkUnroll], span[kChunkUnroll];  // span: first | end << 8 of the valid ids
 #pragma unroll
         for (int u = 0; u < kChunkUnroll; ++u) {
           const uint32_t cc = c + u;
-          vm[u] = 0u;
-          tb[u] = 0u;
+          span[u] = 0u;
+          tok0[u] = 0u;
           v[u] = make_uint4(0u, 0u, 0u, 0u);
           if (cc < ce) {
             while (cc >= pre[r + 1]) ++r;
@@ -155,29 +155,38 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 7) k_match_csr(DevHeader* hd
             const uint32_t k = cc - pre[r];  // chunk index within the run
             const int32_t first = int32_t((e.y >> 16) & 7u) - int32_t(8u * k);  // ids before the run
             const int32_t end = first + int32_t(e.y & 0xffffu);
-            tb[u] = uint32_t(lo_b) + ((e.y >> 19) & 15u) * kCsrSeg;
-            const int32_t lim = min(hi - int32_t(tb[u]), 65535);
-            const uint32_t m = (0xffu << max(first, 0)) & (0xffu >> (8 - min(end, 8)));
-            vm[u] = lim > 0 ? (m & 0xffu) | (uint32_t(lim) << 8) : 0u;
+            span[u] = uint32_t(max(first, 0)) | (uint32_t(min(end, 8)) << 8);
+            tok0[u] = uint32_t(lo_b) + ((e.y >> 19) & 15u) * kCsrSeg;
             v[u] = __ldg(cbase + e.x + k);
           }
         }
+        uint32_t dup = 0;
 #pragma unroll
         for (int u = 0; u < kChunkUnroll; ++u)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
-            const uint32_t id = (word >> (16 * (q & 1))) & 0xffffu;
-            if (((vm[u] >> q) & 1u) && id < (vm[u] >> 8)) {
-              const uint32_t tok = tb[u] + id;
+            const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
+            if (uint32_t(q) >= (span[u] & 0xffu) && uint32_t(q) < (span[u] >> 8) && tok < uint32_t(hi)) {
               if (bytes) {
                 atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
               } else {
                 const uint32_t bit = 1u << (tok & 31);
-                if (atomicOr(&seen1[tok >> 5], bit) & bit) atomicOr(&seen2[tok >> 5], bit);
+                if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1u << (u * 8 + q);
               }
             }
           }
+        if (dup) {
+#pragma unroll
+          for (int u = 0; u < kChunkUnroll; ++u)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if ((dup >> (u * 8 + q)) & 1u) {
+                const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
+                const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
+                atomicOr(&seen2[tok >> 5], 1u << (tok & 31));
+              }
+        }
       }
     }
     // tokens appended after the build that have left the window: compare codes
@@ -227,8 +236,6 @@ cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, cons
   const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
   const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 12 + 4 + size_t(g.L) * 2 + 16;
   cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  // seven CTAs of ~30 KB per SM keep the 1024 heads of the long-context step in one wave
-  cudaFuncSetAttribute(k_match_csr, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   k_match_csr<<<g.queries, kMatchWarps * 32, smem, st>>>(t.hdr, dp.qcodes, t.codes, t.off, t.ids, dp.lists,
                                                          dp.list_len, dp.sample_count, dp.counters, n, g.s, g.w, g.L,
                                                          g.nb, g.cap, g.nseg, g.group, g.threshold);
@@ -350,7 +357,7 @@ __global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) 
     const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
     const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
     float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
-    int threshold, int P, int queries) {
+    int threshold, int P, int queries, uint32_t* status) {
   constexpr int VE = 16 / int(sizeof(T));  // elements per 16-byte slice
   constexpr int LPR = D / VE;              // lanes per row
   constexpr int RPI = 32 / LPR;            // rows per warp-wide load
@@ -431,6 +438,8 @@ __global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) 
     for (int u = 0; u < U; ++u) {
       const int e = e0 + u * RPI;
       ent[u] = e < cn ? sl[e] : 0xffffffffu;
+      // a list entry names a token of the unit's rows [0, capacity)
+      if (ent[u] != 0xffffffffu && !in_range((ent[u] & ~kExactFlag) < uint32_t(cap), status)) ent[u] = 0xffffffffu;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -467,7 +476,10 @@ __global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) 
     float rnum = rqd;  // the cosine's numerator: q.(k - c), or (q - c).(k - c)
     if constexpr (CQ) rnum -= reduce_rows8<LPR>(sc, lane);
     const int je = gi * GR + ju * RPI + sub;
-    const uint32_t rent = je < cn ? sl[je] : 0xffffffffu;
+    uint32_t rent = je < cn ? sl[je] : 0xffffffffu;
+#if MP_CHECK
+    if ((rent & ~kExactFlag) >= uint32_t(cap)) rent = 0xffffffffu;  // skipped above, recorded there
+#endif
     float lg = -CUDART_INF_F;
     if (rent != 0xffffffffu) {
       lg = (rqd + qc) * scale;  // q.k / sqrt(d)
@@ -623,7 +635,7 @@ static cudaError_t launch_attend_t(const Geometry& g, int splits, const TablesPt
   k_attend_gather<T, D, CQ><<<grid, kAttThreads, 0, st>>>(
       dp.lists, dp.list_len, t.center, static_cast<const T*>(keys), static_cast<const T*>(values),
       static_cast<const T*>(q), out, dp.partials, dp.counters, g.cap, g.group, g.K, g.L, g.threshold, splits,
-      g.queries);
+      g.queries, &t.hdr->status);
   return cudaGetLastError();
 }
 

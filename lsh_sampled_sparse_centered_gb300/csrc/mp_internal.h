@@ -138,7 +138,27 @@ cudaError_t launch_attend(const Geometry& g, int n, int splits, const TablesPtrs
 
 int device_sm_count();
 
+// MP_CHECK=1 builds the bounds-checking library: kernels test every index that comes
+// from data (codes, bucket offsets, list entries) against its buffer before using it,
+// record a failure in the status word (MP_STATUS_BAD_INDEX) and skip that access. In
+// the ordinary build the tests compile away.
+#ifndef MP_CHECK
+#define MP_CHECK 0
+#endif
+
 #ifdef __CUDACC__
+// true when `ok`; in the bounds-checking build a false `ok` also sets MP_STATUS_BAD_INDEX
+__device__ __forceinline__ bool in_range(bool ok, uint32_t* status) {
+#if MP_CHECK
+  if (!ok) atomicOr(status, MP_STATUS_BAD_INDEX);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -167,3 +167,23 @@ def test_auto_match_mode_picks_the_fewer_bytes(mp):
     assert mp.mp_tables_layout_get(small).match_mode == mp.MP_MATCH_SCAN
     forced = _cfg(mp, kv_heads=1, q_heads=64, K=1, L=8, capacity=2048, match_mode=mp.MP_MATCH_CSR)
     assert mp.mp_tables_layout_get(forced).match_mode == mp.MP_MATCH_CSR
+
+
+def test_bounds_checking_build_exports_the_same_entry_points(mp):
+    """The MP_CHECK=1 library (built on request) declares and exports what the ordinary one
+    does, and refuses the same bad arguments before any launch."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_mp_build", os.path.join(os.path.dirname(mp.__file__), "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    path = b.build(check=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s+(mp_\w+)", out))
+    assert set(_declared()) <= exported
+    lib = ctypes.CDLL(path)
+    c = _cfg(mp)
+    lib.mp_config_check.argtypes = [ctypes.POINTER(mp.mp_config)]
+    assert lib.mp_config_check(ctypes.byref(c)) == mp.MP_OK
+    c.K = 13
+    assert lib.mp_config_check(ctypes.byref(c)) == mp.MP_ERR_UNSUPPORTED
