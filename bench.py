@@ -239,10 +239,10 @@ class Job:
 
     @property
     def launches_per_job(self):
-        # prepare_w, center (2 kernels), hash keys, csr build; per step: one hash launch
-        # (the appended keys, which also marks the appended end, with the queries), match,
-        # attend
-        return 5 + self.wl.steps * 3
+        # prepare_w, center (partial sums, mean, -W^T c), hash keys, csr build; per step: one
+        # hash launch (the appended keys, which also marks the appended end, with the
+        # queries), match, attend
+        return 6 + self.wl.steps * 3
 
 
 def decode_state_stats(job, torch):

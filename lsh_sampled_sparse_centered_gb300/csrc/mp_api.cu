@@ -231,9 +231,11 @@ static bool rows_on_tensor_cores(const Geometry& g, const TablesPtrs& t) {
 }
 
 // Number of slices per query head for the attention: about 1024 list entries per
-// slice (estimated from the closed-form budget at p = 1/2), at most kSplitsMax. The
-// attention kernel is persistent and takes slices from a work queue, so slices only
-// need to be many enough to spread the long lists over the SMs.
+// slice (estimated from the closed-form budget at p = 1/2), and at least enough slices
+// for two work items per resident CTA of the persistent grid (four per SM) when there
+// are few query heads, as long as a slice keeps ~128 entries; at most kSplitsMax. The
+// attention kernel takes slices from a work queue, so slices only need to be many
+// enough to spread the lists over the SMs.
 static int choose_splits(const Geometry& g, int n) {
   const double x = std::ldexp(1.0, -g.K);
   double frac;
@@ -243,6 +245,8 @@ static int choose_splits(const Geometry& g, int n) {
   const int hi = std::max(lo, n - g.w);
   const double est = double(n - (hi - lo)) + frac * double(hi - lo);
   int s = int(std::ceil(est / 1024.0));
+  const int fill = int((2 * 4 * int64_t(device_sm_count()) + g.queries - 1) / g.queries);
+  s = std::max(s, std::min(fill, int(est / 128.0)));
   if (s < 1) s = 1;
   if (s > kSplitsMax) s = kSplitsMax;
   return s;

@@ -23,6 +23,7 @@ namespace mp {
 // ascending token order, then the exact tokens (bit 31 set).
 constexpr int kMatchWarps = 8;
 constexpr int kChunkUnroll = 4;  // 16-byte chunks of ids in flight per thread
+static_assert(kChunkUnroll * 8 <= 32, "one bit per id slot of the chunks in flight in a 32-bit mask");
 
 // Exclusive scan of v[0..n) in place by the whole block; v[n] receives the total.
 __device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {

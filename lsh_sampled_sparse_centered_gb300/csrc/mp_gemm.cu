@@ -163,12 +163,17 @@ __device__ __forceinline__ void epi_tile_k(uint32_t tbase, uint16_t* codes, int6
     constexpr int C0 = TL0 * KC, C1 = TL1 * KC;
     constexpr int CH0 = C0 / 32, CH1 = (C1 - 1) / 32, NCH = CH1 - CH0 + 1;
     uint32_t words[NCH + 1];
+    // three 32-column loads in flight per wait
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      uint32_t r0[32];
+    for (int i = 0; i < NCH; i += 3) {
+      uint32_t r0[32], r1[32], r2[32];
       tmem_ld32(tbase + uint32_t((CH0 + i) * 32), r0);
+      if (i + 1 < NCH) tmem_ld32(tbase + uint32_t((CH0 + i + 1) * 32), r1);
+      if (i + 2 < NCH) tmem_ld32(tbase + uint32_t((CH0 + i + 2) * 32), r2);
       tmem_wait_ld();
       words[i] = sign_word(r0);
+      if (i + 1 < NCH) words[i + 1] = sign_word(r1);
+      if (i + 2 < NCH) words[i + 2] = sign_word(r2);
     }
     words[NCH] = 0u;
     constexpr uint32_t MASK = (1u << KC) - 1u;
@@ -679,7 +684,16 @@ cudaError_t launch_rows_tc(const Geometry& g, const RowsHashTc& h0, const RowsHa
     a.set[1].nr32 = 0;
   }
   a.vrows = a.set[0].nr32 + a.set[1].nr32;
-  a.nr = std::min(256, a.vrows);
+  // rows per CTA: the largest of 256, 128, 64, 32 whose grid still covers every SM
+  // (every CTA loads a whole W tile, so fewer, fuller CTAs move fewer bytes when the
+  // grid is large enough; with few groups and many rows, smaller row blocks spread
+  // the work)
+  a.nr = 32;
+  for (int cand = 256; cand >= 32; cand >>= 1)
+    if (int64_t((a.vrows + cand - 1) / cand) * g.nt * h0.groups >= device_sm_count()) {
+      a.nr = std::min(cand, a.vrows);
+      break;
+    }
   a.groups_per_w = h0.groups_per_w;
   a.w_rows = g.w_per_layer ? 3 * g.kltc : 0;
   a.kltc = g.kltc;

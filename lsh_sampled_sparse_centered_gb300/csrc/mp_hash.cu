@@ -114,52 +114,82 @@ __global__ void __launch_bounds__(256) k_center_parts(const T* __restrict__ keys
   }
 }
 
-__global__ void k_center_final(const float* __restrict__ cparts, float* __restrict__ center,
-                               __nv_bfloat16* __restrict__ beta, __nv_bfloat16* __restrict__ ones,
-                               float* __restrict__ negbeta,
-                               const float* __restrict__ wt32, int tc, int d,
-                               int kltc, int parts, int count, int units_per_w, int64_t w_stride,
-                               DevHeader* hdr, int n_prefill, int no_center) {
-  extern __shared__ float c[];  // [d]
+// The mean key of each unit from its partial sums (fixed summation order), and the
+// header fields of a built table set.
+__global__ void k_center_mean(const float* __restrict__ cparts, float* __restrict__ center, int d, int parts,
+                              int count, DevHeader* hdr, int n_prefill, int no_center) {
   const int u = blockIdx.x;
   for (int dim = threadIdx.x; dim < d; dim += blockDim.x) {
     float s = 0.f;
     for (int p = 0; p < parts; ++p) s += cparts[(int64_t(u) * parts + p) * d + dim];
-    const float v = (count > 0 && !no_center) ? s / float(count) : 0.f;
-    c[dim] = v;
-    center[int64_t(u) * d + dim] = v;
-  }
-  __syncthreads();
-  // -beta = -W^T c (fp32 W) in tensor-core column order as three bf16 terms hi + mid + lo
-  // (each the bf16 rounding of what is left), an exact split of the fp32 value: the
-  // tensor-core hash adds them through one extra K step against rows of ones
-  if (tc) {
-    const float* w = wt32 + int64_t(u / units_per_w) * w_stride;
-    for (int j = threadIdx.x; j < kltc; j += blockDim.x) {
-      const float* row = w + int64_t(j) * d;
-      float sacc = 0.f;
-      for (int dim = 0; dim < d; ++dim) sacc = fmaf(row[dim], c[dim], sacc);
-      const float nb = -sacc;
-      negbeta[int64_t(u) * kltc + j] = nb;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(nb);
-      const float r1 = nb - __bfloat162float(hi);
-      const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-      __nv_bfloat16* o = beta + (int64_t(u) * kltc + j) * 16;
-      o[0] = hi;
-      o[1] = mid;
-      o[2] = lo;
-      for (int k = 3; k < 16; ++k) o[k] = __float2bfloat16_rn(0.f);
-    }
-    if (u == 0)
-      for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x)
-        ones[i] = __float2bfloat16_rn((i & 15) < 3 ? 1.f : 0.f);
+    center[int64_t(u) * d + dim] = (count > 0 && !no_center) ? s / float(count) : 0.f;
   }
   if (u == 0 && threadIdx.x == 0) {
     hdr->n_prefill = n_prefill;
     hdr->appended_end = n_prefill;
     __threadfence();
     hdr->magic = kMagic;
+  }
+}
+
+// -beta = -W^T c (fp32 W) for kBetaUnits units x 128 tensor-core columns per CTA, in
+// tile-aligned column order, stored as fp32 and as three bf16 terms hi + mid + lo (each
+// the bf16 rounding of what is left, an exact split of the fp32 value): the tensor-core
+// hash adds them through one extra K step against rows of ones. Thread j owns column
+// j of the block and reads its W row once per W matrix met in the unit tile.
+constexpr int kBetaUnits = 16;
+constexpr int kBetaCols = 128;
+
+__global__ void __launch_bounds__(kBetaCols, 4) k_center_beta(const float* __restrict__ center,
+                                                          __nv_bfloat16* __restrict__ beta,
+                                                          __nv_bfloat16* __restrict__ ones,
+                                                          float* __restrict__ negbeta, const float* __restrict__ wt32,
+                                                          int units, int d, int kltc, int units_per_w,
+                                                          int64_t w_stride) {
+  extern __shared__ float cs[];  // [kBetaUnits][d]
+  const int u0 = blockIdx.x * kBetaUnits;
+  const int nu = min(kBetaUnits, units - u0);
+  for (int i = threadIdx.x; i < nu * d; i += blockDim.x) cs[i] = center[int64_t(u0) * d + i];
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) ones[i] = __float2bfloat16_rn((i & 15) < 3 ? 1.f : 0.f);
+  __syncthreads();
+  const int j = blockIdx.y * kBetaCols + threadIdx.x;
+  if (j >= kltc) return;
+  float acc[kBetaUnits];
+#pragma unroll
+  for (int i = 0; i < kBetaUnits; ++i) acc[i] = 0.f;
+  // units of the tile that share a W matrix are done together, one pass over the W row
+  for (int ua = 0; ua < nu;) {
+    const int wi = (u0 + ua) / units_per_w;
+    const int ub = min(nu, (wi + 1) * units_per_w - u0);  // first unit of the next W matrix
+    const float4* row = reinterpret_cast<const float4*>(wt32 + int64_t(wi) * w_stride + int64_t(j) * d);
+    for (int q = 0; q < d / 4; ++q) {
+      const float4 w = __ldg(row + q);
+#pragma unroll
+      for (int i = 0; i < kBetaUnits; ++i)
+        if (i >= ua && i < ub) {
+          const float4 c = reinterpret_cast<const float4*>(cs + i * d)[q];
+          acc[i] = fmaf(w.x, c.x, fmaf(w.y, c.y, fmaf(w.z, c.z, fmaf(w.w, c.w, acc[i]))));
+        }
+    }
+    ua = ub;
+  }
+#pragma unroll
+  for (int i = 0; i < kBetaUnits; ++i) {
+    if (i >= nu) continue;
+    const int64_t u = u0 + i;
+    const float nb = -acc[i];
+    negbeta[u * kltc + j] = nb;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(nb);
+    const float r1 = nb - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    __nv_bfloat16* o = beta + (u * kltc + j) * 16;
+    o[0] = hi;
+    o[1] = mid;
+    o[2] = lo;
+#pragma unroll
+    for (int k = 3; k < 16; ++k) o[k] = __float2bfloat16_rn(0.f);
   }
 }
 
@@ -177,11 +207,15 @@ cudaError_t launch_center(const Geometry& g, const void* keys, int n_prefill, co
         static_cast<const float*>(keys), t.cparts, g.d, g.cap, lo, hi, g.parts);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
-  k_center_final<<<g.units, 256, g.d * sizeof(float), st>>>(t.cparts, t.center, t.beta, t.ones, t.negbeta, t.wt32,
-                                                          t.wt16 != nullptr, g.d,
-                                                          g.kltc, g.parts, hi - lo, g.batch * g.kvh,
-                                                          w_stride, t.hdr, n_prefill, g.no_center);
+  k_center_mean<<<g.units, 128, 0, st>>>(t.cparts, t.center, g.d, g.parts, hi - lo, t.hdr, n_prefill, g.no_center);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // -beta only for the tensor-core paths (bf16 configurations)
+  if (t.wt16 && g.kltc > 0) {
+    const int64_t w_stride = g.w_per_layer ? int64_t(g.kltc) * g.d : 0;
+    dim3 gb((g.units + kBetaUnits - 1) / kBetaUnits, (g.kltc + kBetaCols - 1) / kBetaCols);
+    k_center_beta<<<gb, kBetaCols, size_t(kBetaUnits) * g.d * sizeof(float), st>>>(
+        t.center, t.beta, t.ones, t.negbeta, t.wt32, g.units, g.d, g.kltc, g.batch * g.kvh, w_stride);
+  }
   return cudaGetLastError();
 }
 
