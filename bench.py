@@ -48,6 +48,11 @@ def parse_args():
                          "(one layer of the workload; one JSON line per grid point)")
     ap.add_argument("--eager", action="store_true",
                     help="launch every call from Python instead of replaying the captured job graph")
+    ap.add_argument("--cone", type=float, default=None,
+                    help="key cone a in k = a·mu + N(0, I), sink -a·mu (the pages' narrow cones: 40 to 80); "
+                         "default: the workload's recipe")
+    ap.add_argument("--center-query", action="store_true",
+                    help="hash the query centered (q - c) and take p from cos(q - c, k - c)")
     return ap.parse_args()
 
 
@@ -161,7 +166,7 @@ class ClockSampler:
 class Job:
     """Buffers of one workload replica on the current GPU and the ABI calls of one job."""
 
-    def __init__(self, mp, wl, device, stream):
+    def __init__(self, mp, wl, device, stream, center_query: bool = False):
         import torch
         import workloads as WL
         self.mp, self.wl, self.dev, self.stream = mp, wl, device, stream
@@ -170,7 +175,8 @@ class Job:
         self.queries = t["queries"]
         self.cfg = mp.make_config(layers=wl.layers, batch=wl.batch, kv_heads=wl.kv_heads, q_heads=wl.q_heads,
                                   head_dim=wl.head_dim, K=wl.K, L=wl.L, n_sink=wl.n_sink, window=wl.window,
-                                  capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer)
+                                  capacity=wl.capacity, dtype=wl.dtype, w_per_layer=wl.w_per_layer,
+                                  center_query=center_query)
         self.tl = mp.mp_tables_layout_get(self.cfg)
         self.dl = mp.mp_decode_layout_get(self.cfg)
         self.tables = torch.empty(self.tl.total_bytes, dtype=torch.uint8, device=device)
@@ -283,9 +289,11 @@ def run_ours(args, rank, world, local):
     wl = wl.replace(seed=wl.seed + 1000 * rank)  # independent replica per rank
     if args.w_fp32:
         wl = wl.replace(w_bf16=False, name=wl.name + "-fp32W")
+    if args.cone is not None:
+        wl = wl.replace(cone=args.cone, sink_scale=1.0, name=wl.name + "-cone%g" % args.cone)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        job = Job(mp, wl, dev, stream)
+        job = Job(mp, wl, dev, stream, center_query=args.center_query)
     torch.cuda.synchronize()
 
     # warm-up (eager), then capture the job into a CUDA graph unless --eager
@@ -367,13 +375,15 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
-        "data": "synthetic: seeded cone keys k=3mu+N(0,I) with sink k0=-6mu, queries q=-2mu+N(0,I), "
+        "data": "synthetic: seeded cone keys k=%gmu+N(0,I) with sink k0=-%gmu, queries q=-2mu+N(0,I), " % (
+            wl.cone, wl.sink_scale * wl.cone) +
                 "values N(0,1), W N(0,1)" + (" rounded to bf16" if wl.w_bf16 else " in fp32"),
         "config": {"workload": wl.name, "layers": wl.layers, "batch": wl.batch, "kv_heads": wl.kv_heads,
                    "q_heads": wl.q_heads, "head_dim": wl.head_dim, "n_prefill": wl.n_prefill,
                    "decode_steps": wl.steps, "K": wl.K, "L": wl.L, "n_sink": wl.n_sink, "window": wl.window,
                    "step": "build tables + %d x (append + decode attention)" % wl.steps,
                    "parallelism": "replicas" if world > 1 else "single",
+                   "query": "centered (q - c)" if args.center_query else "as is",
                    "launch": launch_mode,
                    "l2": ("inputs larger than L2 (%.1f GB of K/V and tables resident)" % (resident / 1e9))
                    if not flush else ("inputs fit in L2 (%.0f MB of K/V and tables): 256 MB written between "

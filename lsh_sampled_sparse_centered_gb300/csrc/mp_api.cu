@@ -231,11 +231,12 @@ static bool rows_on_tensor_cores(const Geometry& g, const TablesPtrs& t) {
 }
 
 // Number of slices per query head for the attention: about 1024 list entries per
-// slice (estimated from the closed-form budget at p = 1/2), and at least enough slices
-// for two work items per resident CTA of the persistent grid (four per SM) when there
-// are few query heads, as long as a slice keeps ~128 entries; at most kSplitsMax. The
+// slice (estimated from the closed-form budget at p = 1/2); when that leaves fewer work
+// items than resident CTAs of the persistent grid (four per SM), enough slices for one
+// item per CTA, as long as a slice keeps ~128 entries; at most kSplitsMax. The
 // attention kernel takes slices from a work queue, so slices only need to be many
-// enough to spread the lists over the SMs.
+// enough to spread the lists over the SMs (more, shorter slices measured slower on
+// grids that were already full: each slice writes and merges a partial).
 static int choose_splits(const Geometry& g, int n) {
   const double x = std::ldexp(1.0, -g.K);
   double frac;
@@ -245,8 +246,11 @@ static int choose_splits(const Geometry& g, int n) {
   const int hi = std::max(lo, n - g.w);
   const double est = double(n - (hi - lo)) + frac * double(hi - lo);
   int s = int(std::ceil(est / 1024.0));
-  const int fill = int((2 * 4 * int64_t(device_sm_count()) + g.queries - 1) / g.queries);
-  s = std::max(s, std::min(fill, int(est / 128.0)));
+  const int64_t resident = 4 * int64_t(device_sm_count());
+  if (int64_t(s) * g.queries < resident) {
+    const int fill = int((resident + g.queries - 1) / g.queries);
+    s = std::max(s, std::min(fill, int(est / 128.0)));
+  }
   if (s < 1) s = 1;
   if (s > kSplitsMax) s = kSplitsMax;
   return s;
