@@ -232,11 +232,12 @@ static bool rows_on_tensor_cores(const Geometry& g, const TablesPtrs& t) {
 
 // Number of slices per query head for the attention: about 1024 list entries per
 // slice (estimated from the closed-form budget at p = 1/2); when that leaves fewer work
-// items than resident CTAs of the persistent grid (four per SM), enough slices for one
-// item per CTA, as long as a slice keeps ~128 entries; at most kSplitsMax. The
-// attention kernel takes slices from a work queue, so slices only need to be many
-// enough to spread the lists over the SMs (more, shorter slices measured slower on
-// grids that were already full: each slice writes and merges a partial).
+// items than resident CTAs of the persistent grid (four per SM), the largest number of
+// slices that still fits in one wave of the grid, as long as a slice keeps ~128 entries;
+// at most kSplitsMax. The time of the launch is about the number of waves times a
+// slice's length, so a slice count that spills into a second wave is slower than the
+// one below it (measured on 256 query heads of 128K tokens: 2 slices 69 us, 3 slices
+// 83 us, 5 slices 76 us).
 static int choose_splits(const Geometry& g, int n) {
   const double x = std::ldexp(1.0, -g.K);
   double frac;
@@ -248,7 +249,7 @@ static int choose_splits(const Geometry& g, int n) {
   int s = int(std::ceil(est / 1024.0));
   const int64_t resident = 4 * int64_t(device_sm_count());
   if (int64_t(s) * g.queries < resident) {
-    const int fill = int((resident + g.queries - 1) / g.queries);
+    const int fill = int(resident / g.queries);  // slices per head of one full wave
     s = std::max(s, std::min(fill, int(est / 128.0)));
   }
   if (s < 1) s = 1;
