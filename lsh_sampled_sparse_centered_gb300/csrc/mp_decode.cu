@@ -303,6 +303,14 @@ constexpr int kAttThreads = 128;
 // registers and the warps of a CTA merge through shared memory at the end.
 // ---------------------------------------------------------------------------------
 constexpr int kGatherUnroll = 8;
+
+// 16 bytes of a K or V row: read-only, and not kept in L1 (the rows are streamed; the
+// query heads that share a row meet it in L2)
+__device__ __forceinline__ uint4 ld_na(const uint4* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 constexpr int kListChunk = 1024;
 
 // a 16-byte slice of a row as packed fp32 pairs: 4 pairs of bf16, or 2 pairs of fp32
@@ -446,8 +454,8 @@ __global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) 
     for (int u = 0; u < U; ++u) {
       if (ent[u] != 0xffffffffu) {
         const int64_t tok = int64_t(ent[u] & ~kExactFlag);
-        kv[u] = __ldg(reinterpret_cast<const uint4*>(kbase + tok * D));
-        vv[u] = __ldg(reinterpret_cast<const uint4*>(vbase + tok * D));
+        kv[u] = ld_na(reinterpret_cast<const uint4*>(kbase + tok * D));
+        vv[u] = ld_na(reinterpret_cast<const uint4*>(vbase + tok * D));
       } else {
         kv[u] = make_uint4(0u, 0u, 0u, 0u);
         vv[u] = make_uint4(0u, 0u, 0u, 0u);
