@@ -356,13 +356,15 @@ __device__ __forceinline__ int row_lane(int sub, int u) {
 }
 
 // CQ (center_query): p = 1 - theta(q - c, k - c)/pi instead of 1 - theta(q, k - c)/pi.
+// bf16 rows run four CTAs per SM in both readings (the centered one then spills 24 bytes
+// and still measured 181 us against 189 us at three per SM on the 32-layer step).
 // Per row the kernel accumulates q.(k - c) and |k - c|^2 (and, for CQ, c.(k - c)); the
 // logit's q.k is q.(k - c) + q.c with q.c constant per head, and the cosine's numerator
 // q.(k - c) (or (q - c).(k - c) = q.(k - c) - c.(k - c)) is formed without subtracting two
 // large dot products, which keeps it accurate when the keys sit far from the origin
 // (narrow key cones).
 template <typename T, int D, bool CQ>
-__global__ void __launch_bounds__(kAttThreads, (sizeof(T) == 2 && !CQ) ? 4 : 3) k_attend_gather(
+__global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_gather(
     const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
     const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
     float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
