@@ -495,62 +495,113 @@ def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
     }
 
 
+def e2e_groups(wl):
+    """How the end-to-end run splits the job so that compute on one part overlaps the
+    host-to-device copy of the next: groups of layers (any number of layers per group
+    that divides them, four groups at most), else groups of sequences when there is one
+    layer, else one group. Returns (dimension, groups) with dimension "layers",
+    "batch" or None."""
+    for dim, size in (("layers", wl.layers), ("batch", wl.batch if wl.layers == 1 else 1)):
+        for g in (4, 2):
+            if size >= g and size % g == 0:
+                return dim, g
+    return None, 1
+
+
 def run_e2e(job, stream, args, world):
     """Same job through the public API with host buffers: pinned host inputs copied in
-    and outputs copied back inside the timed region."""
+    and outputs copied back inside the timed region. The job is issued in groups of
+    layers (or sequences): one copy stream moves each group's keys and W, then its values
+    and queries, in order; each group's build and decode steps start as soon as its own
+    inputs have landed, and its outputs go back on a second copy stream while the next
+    group computes."""
     import torch
-    h_keys = torch.empty(job.keys.shape, dtype=job.keys.dtype, pin_memory=True)
-    h_vals = torch.empty(job.values.shape, dtype=job.values.dtype, pin_memory=True)
-    h_W = torch.empty(job.W.shape, dtype=job.W.dtype, pin_memory=True)
-    h_q = torch.empty(job.queries.shape, dtype=job.queries.dtype, pin_memory=True)
-    h_out = torch.empty(job.outs.shape, dtype=job.outs.dtype, pin_memory=True)
-    h_keys.copy_(job.keys)
-    h_vals.copy_(job.values)
-    h_W.copy_(job.W)
-    h_q.copy_(job.queries)
-    d_keys = torch.empty_like(job.keys)
-    d_vals = torch.empty_like(job.values)
-    d_W = torch.empty_like(job.W)
-    d_q = torch.empty_like(job.queries)
+    mp, wl = job.mp, job.wl
+    dim, ng = e2e_groups(wl)
+    per = (wl.layers if dim == "layers" else wl.batch if dim == "batch" else 1) // ng
+
+    def part(t, i, lead=0):
+        """Group i of a tensor whose layer dimension is `lead` (its batch dimension is
+        lead + 1)."""
+        if dim is None:
+            return t
+        return t.narrow(lead if dim == "layers" else lead + 1, i * per, per)
+
+    def pinned(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    w_grouped = dim == "layers" and wl.w_per_layer
+    # per group: keys, values (and W) are contiguous slices; queries and outputs get
+    # buffers of their own so that every copy is one dense block
+    h_keys, h_vals, h_W = pinned(job.keys), pinned(job.values), pinned(job.W)
+    h_q = [pinned(part(job.queries, i, lead=1).contiguous()) for i in range(ng)]
+    h_out = [torch.empty(q.shape, dtype=torch.float32, pin_memory=True) for q in h_q]
+    d_keys, d_vals, d_W = torch.empty_like(job.keys), torch.empty_like(job.values), torch.empty_like(job.W)
+    d_q = [torch.empty(q.shape, dtype=q.dtype, device=job.dev) for q in h_q]
+    d_out = [torch.empty(q.shape, dtype=torch.float32, device=job.dev) for q in h_q]
+    gcfg = mp.make_config(layers=per if dim == "layers" else wl.layers, batch=per if dim == "batch" else wl.batch,
+                          kv_heads=wl.kv_heads, q_heads=wl.q_heads, head_dim=wl.head_dim, K=wl.K, L=wl.L,
+                          n_sink=wl.n_sink, window=wl.window, capacity=wl.capacity, dtype=wl.dtype,
+                          w_per_layer=wl.w_per_layer, center_query=bool(job.cfg.center_query))
+    gtl, gdl = mp.mp_tables_layout_get(gcfg), mp.mp_decode_layout_get(gcfg)
+    g_tables = [torch.empty(gtl.total_bytes, dtype=torch.uint8, device=job.dev) for _ in range(ng)]
+    g_scratch = [torch.empty(gdl.total_bytes, dtype=torch.uint8, device=job.dev) for _ in range(ng)]
     torch.cuda.synchronize()
+    up = torch.cuda.Stream(device=job.dev)
+    down = torch.cuda.Stream(device=job.dev)
 
-    graph, job.graph = job.graph, None
-    # host -> device copies in 256 MB pieces spread over eight copy streams (the host
-    # link takes several copies at once); the build waits for the keys and W only, so
-    # the values' copy overlaps it, and the decode steps wait for the values
-    copy_streams = [torch.cuda.Stream(device=job.dev) for _ in range(8)]
-    piece = 256 << 20
+    def copy_on(s, dst, src):
+        with torch.cuda.stream(s):
+            dst.copy_(src, non_blocking=True)
 
-    def h2d(dst, src, events):
-        d, h = dst.view(-1).view(torch.uint8), src.view(-1).view(torch.uint8)
-        for i, o in enumerate(range(0, d.numel(), piece)):
-            cs = copy_streams[i % len(copy_streams)]
-            with torch.cuda.stream(cs):
-                d[o: o + piece].copy_(h[o: o + piece], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(cs)
-                events.append(ev)
+    def mark(s):
+        e = torch.cuda.Event()
+        e.record(s)
+        return e
 
-    def one():
-        for cs in copy_streams:
-            cs.wait_stream(stream)  # previous job done with the device buffers
+    def one(compute=True):
+        up.wait_stream(stream)  # the previous job is done with the device buffers
+        up.wait_stream(down)
         ev_build, ev_decode = [], []
-        h2d(d_keys, h_keys, ev_build)
-        h2d(d_W, h_W, ev_build)
-        h2d(d_q, h_q, ev_decode)
-        h2d(d_vals, h_vals, ev_decode)
-        for ev in ev_build:
-            stream.wait_event(ev)
-        job.build(keys=d_keys, W=d_W)
-        for ev in ev_decode:
-            stream.wait_event(ev)
-        job.decode_steps(keys=d_keys, values=d_vals, queries=d_q)
-        h_out.copy_(job.outs, non_blocking=True)
+        for i in range(ng):
+            copy_on(up, part(d_keys, i), part(h_keys, i))
+            if w_grouped or i == 0:
+                copy_on(up, part(d_W, i) if w_grouped else d_W, part(h_W, i) if w_grouped else h_W)
+            ev_build.append(mark(up))
+            copy_on(up, part(d_vals, i), part(h_vals, i))
+            copy_on(up, d_q[i], h_q[i])
+            ev_decode.append(mark(up))
+        for i in range(ng):
+            if not compute:
+                stream.wait_event(ev_decode[i])
+                down.wait_event(mark(stream))
+                copy_on(down, h_out[i], d_out[i])
+                continue
+            keys_i, vals_i = part(d_keys, i), part(d_vals, i)
+            stream.wait_event(ev_build[i])
+            mp.mp_build_tables(gcfg, keys_i, wl.n_prefill, part(d_W, i) if w_grouped else d_W, g_tables[i],
+                               stream=job.sp)
+            stream.wait_event(ev_decode[i])
+            for s_ in range(wl.steps):
+                n = wl.seq_len(s_)
+                if wl.append:
+                    mp.mp_decode_step(gcfg, g_tables[i], keys_i, vals_i, n - 1, d_q[i][s_], d_out[i][s_],
+                                      g_scratch[i], scratch_bytes=gdl.total_bytes, stream=job.sp)
+                else:
+                    mp.mp_decode_attention(gcfg, g_tables[i], keys_i, vals_i, n, d_q[i][s_], d_out[i][s_],
+                                           g_scratch[i], scratch_bytes=gdl.total_bytes, stream=job.sp)
+            down.wait_event(mark(stream))
+            copy_on(down, h_out[i], d_out[i])
+        stream.wait_stream(down)
 
     n = max(1, min(args.steps, 3))
     with torch.cuda.stream(stream):
         one()
     torch.cuda.synchronize()
+    for t in g_tables:
+        assert (mp.mp_get_status(t, stream=job.sp) & ~mp.MP_STATUS_W_NOT_BF16) == 0
     barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -561,12 +612,22 @@ def run_e2e(job, stream, args, world):
     torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, True) / n
-    bi = sum(t.numel() * t.element_size() for t in (h_keys, h_vals, h_W, h_q))
-    bo = h_out.numel() * h_out.element_size()
-    del d_keys, d_vals, d_W, d_q
-    job.graph = graph
+    # the same copies with no compute: what the host link alone takes per job
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            one(compute=False)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    copy_ms = max_over_ranks(ev0.elapsed_time(ev1), world, True) / n
+    bi = sum(t.numel() * t.element_size() for t in [h_keys, h_vals, h_W] + h_q)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+    del d_keys, d_vals, d_W, d_q, d_out, g_tables, g_scratch
     return {"value": job.queries_per_job * world / (ms / 1e3), "unit": "queries/s", "ms_per_step": ms,
-            "steps": n, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "steps": n, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "copies_alone_ms": copy_ms, "host_link_gbs": (bi + bo) / (copy_ms / 1e3) / 1e9,
+            "overlap": ("%d groups of %s, each built and decoded as soon as its inputs land" % (ng, dim))
+            if dim else "none (one group)"}
 
 
 # ----------------------------------------------------------------------------------
