@@ -8,23 +8,26 @@
 
 namespace mp {
 
-// Called by all 256 threads of a block. `sel` may live in shared or global memory;
-// word i covers tokens 32i .. 32i+31. If !valid, S is empty.
+// Called by all threads of a block (a multiple of 32, at most 256). `sel` may live in
+// shared or global memory; word i covers tokens origin + 32i .. origin + 32i + 31
+// (origin <= lo). If !valid, S is empty.
 __device__ __forceinline__ void write_list(const uint32_t* sel, bool valid, int lo, int hi, int n,
-                                           uint32_t* lst, int32_t* sample_count, int32_t* list_len) {
+                                           uint32_t* lst, int32_t* sample_count, int32_t* list_len,
+                                           int origin = 0) {
   __shared__ int wsum[8];
   __shared__ int s_total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwords = (hi + 31) >> 5;
-  const int w0 = lo >> 5;
+  const int rl = lo - origin, rh = hi - origin;  // the region in bit positions of sel
+  const int nwords = (rh + 31) >> 5;
+  const int w0 = rl >> 5;
   const int nw = nwords - w0;
   const int per = (nw + blockDim.x - 1) / blockDim.x;
   const int my0 = w0 + threadIdx.x * per, my1 = min(nwords, my0 + per);
   auto word_at = [&](int wi) -> uint32_t {
     uint32_t v = sel[wi];
     const int base = wi << 5;
-    if (base < lo) v &= ~((1u << (lo - base)) - 1u);  // lo - base in 1..31
-    if (base + 32 > hi) v &= (1u << (hi - base)) - 1u; // hi - base in 1..31
+    if (base < rl) v &= ~((1u << (rl - base)) - 1u);  // rl - base in 1..31
+    if (base + 32 > rh) v &= (1u << (rh - base)) - 1u; // rh - base in 1..31
     return v;
   };
   int local = 0;
@@ -40,7 +43,7 @@ __device__ __forceinline__ void write_list(const uint32_t* sel, bool valid, int 
   __syncthreads();
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < int(blockDim.x >> 5); ++i) {
       const int v = wsum[i];
       wsum[i] = run;
       run += v;
@@ -55,7 +58,7 @@ __device__ __forceinline__ void write_list(const uint32_t* sel, bool valid, int 
       while (v) {
         const int b = __ffs(v) - 1;
         v &= v - 1;
-        lst[pos++] = uint32_t((wi << 5) + b);
+        lst[pos++] = uint32_t(origin + (wi << 5) + b);
       }
     }
   }

@@ -17,13 +17,15 @@ namespace mp {
 // ---------------------------------------------------------------------------------
 // sampled set: one CTA per query head
 // ---------------------------------------------------------------------------------
-// Bitmaps over token ids [0, n - window): `seen1` marks tokens met in >= 1 table's
-// bucket, `seen2` in >= 2. With threshold 2 the sampled set is seen2 restricted to
-// [n_sink, n - window); with threshold 1 it is seen1. Compaction writes S in
-// ascending token order, then the exact tokens (bit 31 set).
+// Bitmaps over the tokens [lo, n), bit j <-> token lo + j (lo = n_sink when the region is
+// not empty): `seen1` marks tokens met in >= 1 table's bucket, `seen2` in >= 2. With
+// threshold 2 the sampled set is seen2 restricted to [lo, n - window); with threshold 1
+// it is seen1. Compaction writes S in ascending token order, then the exact tokens (bit
+// 31 set). The bitmaps reach n rather than n - window so that a bucketed token (always
+// < n_prefill <= n in a decode that covers the prefill) needs no range test; the window
+// bits are masked off by the compaction.
 constexpr int kMatchWarps = 8;
-constexpr int kChunkUnroll = 4;  // 16-byte chunks of ids in flight per thread
-static_assert(kChunkUnroll * 8 <= 32, "one bit per id slot of the chunks in flight in a 32-bit mask");
+constexpr int kChunkUnroll = 2;  // 16-byte chunks of ids in flight per thread
 
 // Exclusive scan of v[0..n) in place by the whole block; v[n] receives the total.
 __device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {
@@ -57,6 +59,76 @@ __device__ __forceinline__ void block_exclusive_scan(uint32_t* v, int n) {
   __syncthreads();
 }
 
+// One thread's share [cb, ce) of a head's id chunks, kChunkUnroll chunks at a time (all
+// loads issued before the first mark). Run r = (table, segment) holds the ids of the
+// query's bucket in that segment; id i of segment sg is token lo + 32768 sg + i, i.e. bit
+// 32768 sg + i of the bitmaps. BYTES: one byte counter per token instead of the two
+// bitmaps (thresholds >= 3). CLIP: drop tokens at or beyond rh (a decode over fewer
+// tokens than the prefill). The bounds-checking build also tests every bit position
+// against the nbits bits of the bitmaps.
+template <bool BYTES, bool CLIP>
+__device__ __forceinline__ void walk_chunks(const uint4* __restrict__ cbase, const uint2* bkt, const uint32_t* pre,
+                                            int r, uint32_t cb, uint32_t ce, uint32_t rh, uint32_t nbits,
+                                            uint32_t* seen1, uint32_t* seen2, uint32_t* cnt, uint32_t* status) {
+  const uint32_t s1 = uint32_t(__cvta_generic_to_shared(seen1));
+  const uint32_t s2off = uint32_t(__cvta_generic_to_shared(seen2)) - s1;
+  for (uint32_t c = cb; c < ce; c += kChunkUnroll) {
+    uint4 v[kChunkUnroll];
+    uint32_t vm[kChunkUnroll], sgb[kChunkUnroll];  // vm: bit q <-> slot q is an id of the run
+#pragma unroll
+    for (int u = 0; u < kChunkUnroll; ++u) {
+      const uint32_t cc = c + u;
+      vm[u] = 0u;
+      sgb[u] = 0u;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (cc < ce) {
+        while (cc >= pre[r + 1]) ++r;
+        const uint2 e = bkt[r];
+        const uint32_t k = cc - pre[r];  // chunk index within the run
+        const int32_t first = int32_t((e.y >> 16) & 7u) - int32_t(8u * k);  // ids before the run
+        const int32_t end = first + int32_t(e.y & 0xffffu);
+        const uint32_t f = uint32_t(max(first, 0)), l = uint32_t(min(end, 8));
+        vm[u] = (0xffu >> (8u - l)) & (0xffu << f);
+        sgb[u] = ((e.y >> 19) & 15u) * uint32_t(kCsrSeg);
+        v[u] = __ldg(cbase + e.x + k);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kChunkUnroll; ++u)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
+        const uint32_t id = (q & 1) ? (word >> 16) : (word & 0xffffu);
+        const uint32_t j = sgb[u] + id;  // bit position
+        uint32_t okm = vm[u] & (1u << q);
+        if (CLIP) okm = (j < rh) ? okm : 0u;
+#if MP_CHECK
+        if (okm && !in_range(j < nbits, status)) okm = 0u;
+#else
+        (void)nbits;
+        (void)status;
+#endif
+        if (BYTES) {
+          if (okm) atomicAdd(&cnt[j >> 2], 1u << (8 * (id & 3u)));
+        } else {
+          // seen1 |= bit; when it was set already, seen2 |= bit (both predicated, no branch)
+          const uint32_t bit = __funnelshift_l(0u, 1u, id);
+          const uint32_t a = s1 + ((j >> 5) << 2);
+          asm volatile(
+              "{\n\t.reg .pred p, q;\n\t.reg .b32 o;\n\t"
+              "setp.ne.b32 p, %2, 0;\n\t"
+              "mov.b32 o, 0;\n\t"
+              "@p atom.shared.or.b32 o, [%0], %1;\n\t"
+              "and.b32 o, o, %1;\n\t"
+              "setp.ne.b32 q, o, 0;\n\t"
+              "@q red.shared.or.b32 [%3], %1;\n\t}" ::"r"(a),
+              "r"(bit), "r"(okm), "r"(a + s2off)
+              : "memory");
+        }
+      }
+  }
+}
+
 __global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hdr,
                                                    const uint16_t* __restrict__ qcodes,
                                                    const uint16_t* __restrict__ codes,
@@ -70,7 +142,7 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hd
   const int unit = qh / group;  // [layer][batch][q_head] -> [layer][batch][kv_head]
   const int lo = min(s, n);
   const int hi = max(lo, n - w);
-  const int nwords = (hi + 31) >> 5;
+  const int nwords = (n - lo + 31) >> 5;  // bitmap words over [lo, n)
   // threshold <= 2: two bitmaps (met in >= 1 table, in >= 2 tables);
   // threshold >= 3: one byte counter per token (L <= 255), then a selection bitmap
   const bool bytes = threshold >= 3;
@@ -102,10 +174,9 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hd
     // of ids each. Every run is covered by the 16-byte chunks that hold it; the chunks of
     // all runs of the head are numbered consecutively (a block scan of the per-run chunk
     // counts) and split evenly over the threads, so each thread has about the same number
-    // of chunks, reads them kChunkUnroll at a time (all loads in flight before their
-    // marks) and marks every id of a chunk itself.
+    // of chunks and marks every id of its chunks itself.
     const int64_t tbase = int64_t(unit) * L;
-    const int lo_b = min(s, n0);  // first token bucketed at build time
+    const int lo_b = min(s, n0);  // first token bucketed at build time (= lo here)
     const int nsu = n0 > lo_b ? (n0 - lo_b + kCsrSeg - 1) / kCsrSeg : 0;
     const int runs = L * nsu;
     const uintptr_t idb = reinterpret_cast<uintptr_t>(ids + tbase * cap);  // the unit's id arrays
@@ -141,77 +212,41 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hd
         else rh = mid;
       }
       const uint4* cbase = reinterpret_cast<const uint4*>(idb16);
-      for (uint32_t c = cb; c < ce; c += kChunkUnroll) {
-        uint4 v[kChunkUnroll];
-        uint32_t tok0[kChunkUnroll], span[kChunkUnroll];  // span: first | end << 8 of the valid ids
-#pragma unroll
-        for (int u = 0; u < kChunkUnroll; ++u) {
-          const uint32_t cc = c + u;
-          span[u] = 0u;
-          tok0[u] = 0u;
-          v[u] = make_uint4(0u, 0u, 0u, 0u);
-          if (cc < ce) {
-            while (cc >= pre[r + 1]) ++r;
-            const uint2 e = bkt[r];
-            const uint32_t k = cc - pre[r];  // chunk index within the run
-            const int32_t first = int32_t((e.y >> 16) & 7u) - int32_t(8u * k);  // ids before the run
-            const int32_t end = first + int32_t(e.y & 0xffffu);
-            span[u] = uint32_t(max(first, 0)) | (uint32_t(min(end, 8)) << 8);
-            tok0[u] = uint32_t(lo_b) + ((e.y >> 19) & 15u) * kCsrSeg;
-            v[u] = __ldg(cbase + e.x + k);
-          }
-        }
-        uint32_t dup = 0;
-#pragma unroll
-        for (int u = 0; u < kChunkUnroll; ++u)
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
-            const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
-            if (uint32_t(q) >= (span[u] & 0xffu) && uint32_t(q) < (span[u] >> 8) && tok < uint32_t(hi)) {
-              if (bytes) {
-                atomicAdd(&cnt[tok >> 2], 1u << (8 * (tok & 3)));
-              } else {
-                const uint32_t bit = 1u << (tok & 31);
-                if (atomicOr(&seen1[tok >> 5], bit) & bit) dup |= 1u << (u * 8 + q);
-              }
-            }
-          }
-        if (dup) {
-#pragma unroll
-          for (int u = 0; u < kChunkUnroll; ++u)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if ((dup >> (u * 8 + q)) & 1u) {
-                const uint32_t word = (q < 2) ? v[u].x : (q < 4) ? v[u].y : (q < 6) ? v[u].z : v[u].w;
-                const uint32_t tok = tok0[u] + ((word >> (16 * (q & 1))) & 0xffffu);
-                atomicOr(&seen2[tok >> 5], 1u << (tok & 31));
-              }
-        }
+      // bucketed tokens lie below n0; with n0 <= n they all have a bit (lo_b = lo)
+      const uint32_t rel_hi = uint32_t(hi - lo), nbits = uint32_t(nwords) * 32u;
+      uint32_t* st = &hdr->status;
+      if (n0 <= n) {
+        if (bytes) walk_chunks<true, false>(cbase, bkt, pre, r, cb, ce, rel_hi, nbits, seen1, seen2, cnt, st);
+        else walk_chunks<false, false>(cbase, bkt, pre, r, cb, ce, rel_hi, nbits, seen1, seen2, cnt, st);
+      } else {
+        if (bytes) walk_chunks<true, true>(cbase, bkt, pre, r, cb, ce, rel_hi, nbits, seen1, seen2, cnt, st);
+        else walk_chunks<false, true>(cbase, bkt, pre, r, cb, ce, rel_hi, nbits, seen1, seen2, cnt, st);
       }
     }
     // tokens appended after the build that have left the window: compare codes
     const int a0 = max(lo, n0), a1 = min(hi, app_end);
-    for (int tok = a0 + warp; tok < a1; tok += 8) {
+    for (int tok = a0 + warp; tok < a1; tok += kMatchWarps) {
       int c = 0;
       for (int t = lane; t < L; t += 32) c += (codes[(tbase + t) * cap + tok] == qc[t]) ? 1 : 0;
 #pragma unroll
       for (int k = 16; k > 0; k >>= 1) c += __shfl_xor_sync(0xffffffffu, c, k);
       if (lane == 0) {
+        const int j = tok - lo;
         if (bytes) {
-          atomicAdd(&cnt[tok >> 2], uint32_t(min(c, 255)) << (8 * (tok & 3)));
+          atomicAdd(&cnt[j >> 2], uint32_t(min(c, 255)) << (8 * (j & 3)));
         } else {
-          const uint32_t bit = 1u << (tok & 31);
-          if (c >= 1) atomicOr(&seen1[tok >> 5], bit);
-          if (c >= 2) atomicOr(&seen2[tok >> 5], bit);
+          const uint32_t bit = 1u << (j & 31);
+          if (c >= 1) atomicOr(&seen1[j >> 5], bit);
+          if (c >= 2) atomicOr(&seen2[j >> 5], bit);
         }
       }
     }
   }
   __syncthreads();
   if (bytes) {
-    // selection bitmap: counter >= threshold (reuses the first nwords words)
-    for (int wi = threadIdx.x; wi < nwords; wi += blockDim.x) {
+    // selection bitmap: counter >= threshold (reuses the first words)
+    const int sw = (hi - lo + 31) >> 5;
+    for (int wi = threadIdx.x; wi < sw; wi += blockDim.x) {
       uint32_t m = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -226,14 +261,13 @@ __global__ void __launch_bounds__(kMatchWarps * 32, 5) k_match_csr(DevHeader* hd
   }
   // compaction of [lo, hi)
   write_list(threshold == 2 ? seen2 : seen1, built, lo, hi, n, lists + int64_t(qh) * cap, &sample_count[qh],
-             &list_len[qh]);
+             &list_len[qh], lo);
 }
 
 cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp,
                              cudaStream_t st) {
-  const int lo = min(g.s, n);
-  const int hi = max(lo, n - g.w);
-  const int nwords = (hi + 31) >> 5;
+  const int lo = std::min(g.s, n);
+  const int nwords = (n - lo + 31) >> 5;
   const int body = g.threshold >= 3 ? nwords * 9 : nwords * 2;
   const size_t smem = size_t(body + 1) * 4 + size_t(g.L) * g.nseg * 12 + 4 + size_t(g.L) * 2 + 16;
   cudaFuncSetAttribute(k_match_csr, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
