@@ -117,6 +117,10 @@ WORKLOADS = {
 # profiling case: the long-context workload cut to 4 layers (K/V 1.6 GB, still larger
 # than L2) so that a multi-pass kernel capture holds a few GB of device memory only
 WORKLOADS[5] = WORKLOADS[2].replace(name="llama8b-4L-gqa32x8-d128-n96k-64steps-bf16", layers=4)
+# profiling case for the sampled-set kernel: the 4-layer job with 256 query heads per layer
+# (group 32), so that one decode step has the 32-layer job's 1024 query heads while the
+# device holds the 4-layer job's few GB
+WORKLOADS[6] = WORKLOADS[5].replace(name="llama8b-4L-gqa256x8-d128-n96k-64steps-bf16", q_heads=256)
 
 
 # ----------------------------------------------------------------------------------
