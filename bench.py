@@ -245,10 +245,10 @@ class Job:
 
     @property
     def launches_per_job(self):
-        # prepare_w, center (partial sums, mean, -W^T c), hash keys, csr build; per step: one
-        # hash launch (the appended keys, which also marks the appended end, with the
-        # queries), match, attend
-        return 6 + self.wl.steps * 3
+        # prepare_w, the -log u table, center (partial sums, mean, -W^T c), hash keys, csr
+        # build; per step: one hash launch (the appended keys, which also marks the appended
+        # end, with the queries), match, attend
+        return 7 + self.wl.steps * 3
 
 
 def decode_state_stats(job, torch):
@@ -451,6 +451,7 @@ def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
         "hash_append": ("flops", 2.0 * steps * U * d * KL),
         "hash_step": ("flops", 2.0 * steps * (U + Q) * d * KL),
         "mark_appended": ("bytes", 0),
+        "logu_lut": ("bytes", (4096 + 1) * 4),
         "hash_query": ("flops", 2.0 * steps * Q * d * KL),
         "match_csr": ("bytes", bucket_entries * 2 + steps * Q * wl.L * (4 * -(-(n0 - s) // 32768) + 2)
                       + list_entries * 4),

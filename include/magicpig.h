@@ -52,8 +52,8 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 3 /* 2: mp_config.no_centering, mp_tables_layout.negbeta_f32, three-term W;
-                            3: mp_config.center_query */
+#define MP_ABI_VERSION 4 /* 2: mp_config.no_centering, mp_tables_layout.negbeta_f32, three-term W;
+                            3: mp_config.center_query; 4: mp_tables_layout.logu_lut */
 
 /* return codes */
 #define MP_OK 0
@@ -141,6 +141,9 @@ typedef struct mp_tables_layout {
                             a bucket is unspecified (CSR mode, else 0) */
   uint64_t planes;       /* uint32 [U][L][K][CW]: bit-planes, word w bit i = bit b of the code of token
                             32w+i (scan mode, else 0); CW = capacity/32 rounded up to a multiple of 4 */
+  uint64_t logu_lut;     /* float [4097]: -log u of the config's (K, L, threshold) at the cosines
+                            -0.5 + 1.49·i/4096 (Eq. 10/11), written by mp_build_tables; the attention
+                            interpolates it and evaluates u directly outside [-0.5, 0.99] */
   int32_t n_buckets;     /* NB */
   int32_t parts;
   int32_t tc_cols;       /* TC */

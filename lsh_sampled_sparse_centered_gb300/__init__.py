@@ -56,7 +56,7 @@ class mp_config(ctypes.Structure):
 class mp_tables_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "total_bytes", "header", "center", "beta", "ones", "negbeta_f32", "wt_f32", "wt_bf16", "center_parts", "codes",
-        "csr_offsets", "csr_ids", "planes")] + [(n, ctypes.c_int32) for n in (
+        "csr_offsets", "csr_ids", "planes", "logu_lut")] + [(n, ctypes.c_int32) for n in (
         "n_buckets", "parts", "tc_cols", "match_mode", "cap_words")]
 
 

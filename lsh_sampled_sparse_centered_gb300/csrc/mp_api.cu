@@ -127,6 +127,8 @@ static void tables_layout(const Geometry& g, mp_tables_layout* o) {
     o->planes = off;
     off = align256(off + U * L * uint64_t(g.K) * g.cw * 4);
   }
+  o->logu_lut = off;
+  off = align256(off + uint64_t(kLutN + 1) * 4);
   o->total_bytes = off;
   o->n_buckets = g.nb;
   o->parts = g.parts;
@@ -176,6 +178,7 @@ static TablesPtrs tables_ptrs(const Geometry& g, void* base) {
   t.off = l.csr_offsets ? reinterpret_cast<uint16_t*>(b + l.csr_offsets) : nullptr;
   t.ids = l.csr_ids ? reinterpret_cast<uint16_t*>(b + l.csr_ids) : nullptr;
   t.planes = l.planes ? reinterpret_cast<uint32_t*>(b + l.planes) : nullptr;
+  t.lut = reinterpret_cast<float*>(b + l.logu_lut);
   return t;
 }
 
@@ -260,12 +263,13 @@ static int choose_splits(const Geometry& g, int n) {
 // ---- optional per-launch event timing ----
 enum KernelId {
   K_PREPARE_W, K_CENTER, K_HASH_KEYS_SIMT, K_HASH_KEYS_TC, K_CSR_BUILD, K_HASH_APPEND, K_MARK_APPENDED,
-  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_PLANES_BUILD, K_PLANES_APPEND, K_SCAN, K_COMPACT, K_HASH_STEP, K_COUNT
+  K_HASH_QUERY, K_MATCH_CSR, K_ATTEND, K_PLANES_BUILD, K_PLANES_APPEND, K_SCAN, K_COMPACT, K_HASH_STEP, K_LOGU_LUT,
+  K_COUNT
 };
 static const char* kKernelNames[K_COUNT] = {"prepare_w", "center", "hash_keys_simt", "hash_keys_tc",
                                             "csr_build", "hash_append", "mark_appended", "hash_query",
                                             "match_csr", "attend", "planes_build", "planes_append",
-                                            "scan", "compact", "hash_step"};
+                                            "scan", "compact", "hash_step", "logu_lut"};
 struct ProfRec {
   int id;
   cudaEvent_t a, b;
@@ -366,6 +370,10 @@ int mp_build_tables(const mp_config* cfg, const void* keys, int32_t n_prefill, c
   {
     ProfScope ps(st, K_PREPARE_W);
     if (launch_prepare_w(g, W, t, st) != cudaSuccess) return MP_ERR_CUDA;
+  }
+  {
+    ProfScope ps(st, K_LOGU_LUT);
+    if (launch_logu_lut(g, t, st) != cudaSuccess) return MP_ERR_CUDA;
   }
   {
     ProfScope ps(st, K_CENTER);

@@ -327,6 +327,70 @@ __device__ __forceinline__ float inclusion_prob(float x, int L, int threshold) {
   return 1.f - head;
 }
 
+// The same probability in double precision, for the -log u table.
+__device__ double inclusion_prob_d(double x, int L, int threshold) {
+  if (x >= 1.0) return 1.0;
+  if (x <= 0.0) return 0.0;
+  const double Lf = double(L);
+  if (threshold <= 1) return -expm1(Lf * log1p(-x));
+  if (L < threshold) return 0.0;
+  const double l1x = log1p(-x);
+  const double r = x / (1.0 - x);
+  const double T = double(threshold);
+  if (Lf * x < 0.5 * T) {
+    // tail sum_{j >= T} C(L, j) x^j (1 - x)^(L - j), term by term
+    double term = exp(lgamma(Lf + 1.0) - lgamma(T + 1.0) - lgamma(Lf - T + 1.0) + T * log(x) + (Lf - T) * l1x);
+    double sum = term;
+    for (int j = threshold; j < L && j < threshold + 64; ++j) {
+      term *= (Lf - double(j)) / double(j + 1) * r;
+      sum += term;
+      if (term < 1e-17 * sum) break;
+    }
+    return sum;
+  }
+  // 1 - sum_{j < T} C(L, j) x^j (1 - x)^(L - j)
+  double term = exp(Lf * l1x);
+  double head = term;
+  for (int j = 0; j < threshold - 1; ++j) {
+    term *= (Lf - double(j)) / double(j + 1) * r;
+    head += term;
+  }
+  return 1.0 - head;
+}
+
+// lut[i] = -log u at the cosine kLutLo + i (kLutHi - kLutLo) / kLutN: p = 1 - acos/pi,
+// x = p^K, u = P[Bin(L, x) >= threshold] (Eq. 10/11), u floored at 1e-30 as in the
+// attention's direct evaluation; the header records which (K, L, threshold) it holds.
+__global__ void k_logu_lut(float* __restrict__ lut, DevHeader* hdr, int K, int L, int threshold) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i <= kLutN) {
+    const double cs = double(kLutLo) + (double(kLutHi) - double(kLutLo)) * double(i) / double(kLutN);
+    const double p = 1.0 - acos(cs) / CUDART_PI;
+    double x = 1.0;
+    for (int k = 0; k < K; ++k) x *= p;
+    lut[i] = float(-log(fmax(inclusion_prob_d(x, L, threshold), 1e-30)));
+  }
+  if (i == 0) hdr->lut_key = lut_key_of(K, L, threshold);
+}
+
+cudaError_t launch_logu_lut(const Geometry& g, const TablesPtrs& t, cudaStream_t st) {
+  k_logu_lut<<<(kLutN + 1 + 127) / 128, 128, 0, st>>>(t.lut, t.hdr, g.K, g.L, g.threshold);
+  return cudaGetLastError();
+}
+
+// -log u evaluated directly (cosines outside the table, or no table for this config)
+__device__ __noinline__ float neg_log_u(float cs, int K, int L, int threshold) {
+  const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
+  // x = p^K by squaring (K <= 12)
+  float x = 1.f, pb = p;
+#pragma unroll
+  for (int bit = 0; bit < 4; ++bit) {
+    if ((K >> bit) & 1) x *= pb;
+    pb *= pb;
+  }
+  return -logf(fmaxf(inclusion_prob(x, L, threshold), 1e-30f));
+}
+
 constexpr int kAttThreads = 128;
 
 // ---------------------------------------------------------------------------------
@@ -401,8 +465,8 @@ template <typename T, int D, bool CQ>
 __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_gather(
     const uint32_t* __restrict__ lists, const int32_t* __restrict__ list_len, const float* __restrict__ center,
     const T* __restrict__ keys, const T* __restrict__ values, const T* __restrict__ q, float* __restrict__ out,
-    float* __restrict__ partials, uint32_t* __restrict__ counters, int cap, int group, int K, int L,
-    int threshold, int P, int queries, uint32_t* status) {
+    float* __restrict__ partials, uint32_t* __restrict__ counters, const float* __restrict__ lut,
+    const DevHeader* hdr, int cap, int group, int K, int L, int threshold, int P, int queries, uint32_t* status) {
   constexpr int VE = 16 / int(sizeof(T));  // elements per 16-byte slice
   constexpr int LPR = D / VE;              // lanes per row
   constexpr int RPI = 32 / LPR;            // rows per warp-wide load
@@ -418,6 +482,11 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
   // work queue (counters[queries], zeroed by the match kernel), so that a CTA that
   // drew short slices takes more of them
   __shared__ int s_item;
+  // the -log u table holds this config's (K, L, threshold) once the tables are built
+  __shared__ float s_lut[kLutN + 1];
+  const bool use_lut = hdr->lut_key == lut_key_of(K, L, threshold);
+  if (use_lut)
+    for (int i = threadIdx.x; i <= kLutN; i += kAttThreads) s_lut[i] = __ldg(lut + i);
   for (;;) {
   if (threadIdx.x == 0) s_item = int(atomicAdd(&counters[queries], 1u));
   __syncthreads();
@@ -534,15 +603,15 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
         const float kn = sqrtf(rkk);
         float cs = (qnorm > 0.f && kn > 0.f) ? rnum / (qnorm * kn) : 0.f;
         cs = fminf(1.f, fmaxf(-1.f, cs));
-        const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
-        // x = p^K by squaring (K <= 12)
-        float x = 1.f, pb = p;
-#pragma unroll
-        for (int bit = 0; bit < 4; ++bit) {
-          if ((K >> bit) & 1) x *= pb;
-          pb *= pb;
+        if (use_lut && cs >= kLutLo && cs <= kLutHi) {
+          // -log u interpolated on the build-time table (staged in shared memory)
+          const float tt = (cs - kLutLo) * (float(kLutN) / (kLutHi - kLutLo));
+          const int i = min(int(tt), kLutN - 1);
+          const float a = s_lut[i], b = s_lut[i + 1];
+          lg += fmaf(tt - float(i), b - a, a);
+        } else {
+          lg += neg_log_u(cs, K, L, threshold);
         }
-        lg -= logf(fmaxf(inclusion_prob(x, L, threshold), 1e-30f));
       }
     }
     // group maximum (every row sits in LPR/8 lanes)
@@ -679,7 +748,7 @@ static cudaError_t launch_attend_t(const Geometry& g, int splits, const TablesPt
   const int grid = int(std::min<int64_t>(items, int64_t(occ) * device_sm_count()));
   k_attend_gather<T, D, CQ><<<grid, kAttThreads, 0, st>>>(
       dp.lists, dp.list_len, t.center, static_cast<const T*>(keys), static_cast<const T*>(values),
-      static_cast<const T*>(q), out, dp.partials, dp.counters, g.cap, g.group, g.K, g.L, g.threshold, splits,
+      static_cast<const T*>(q), out, dp.partials, dp.counters, t.lut, t.hdr, g.cap, g.group, g.K, g.L, g.threshold, splits,
       g.queries, &t.hdr->status);
   return cudaGetLastError();
 }

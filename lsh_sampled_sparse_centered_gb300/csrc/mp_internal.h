@@ -26,7 +26,8 @@ struct DevHeader {
   uint32_t status;       // MP_STATUS_* bits
   uint32_t w_terms3;     // nonzero: W is not bf16-representable, the tensor-core paths add
                          // the mid and lo bf16 terms of the split W = hi + mid + lo
-  int32_t pad[59];
+  uint32_t lut_key;      // (K, L, threshold) the -log u table was written for (lut_key_of)
+  int32_t pad[58];
 };
 static_assert(sizeof(DevHeader) == 256, "header size");
 
@@ -63,7 +64,18 @@ struct TablesPtrs {
   uint16_t* off;   // [U][L][nseg][nb+1]
   uint16_t* ids;   // [U][L][cap]
   uint32_t* planes;
+  float* lut;  // [kLutN + 1]: -log u on the cosine grid kLutLo + i (kLutHi - kLutLo) / kLutN
 };
+
+// -log u as a table over the cosine of the hashed query with k - c (written at build
+// time, interpolated by the attention): kLutN intervals on [kLutLo, kLutHi]. Outside
+// that range (u near 0 below it; the square-root edge of 1 - acos(c)/pi at c = 1 above
+// it) the attention evaluates u directly.
+constexpr int kLutN = 4096;
+constexpr float kLutLo = -0.5f, kLutHi = 0.99f;
+__host__ __device__ constexpr uint32_t lut_key_of(int K, int L, int threshold) {
+  return 0x80000000u | uint32_t(K) | (uint32_t(L) << 8) | (uint32_t(threshold) << 20);
+}
 
 struct DecodePtrs {
   uint16_t* qcodes;
@@ -126,6 +138,7 @@ cudaError_t launch_hash_keys_tc(const Geometry& g, const void* keys, int n_prefi
                                 cudaStream_t st, bool* used);
 cudaError_t launch_csr_build(const Geometry& g, int n_prefill, const TablesPtrs& t, cudaStream_t st);
 cudaError_t launch_mark_appended(const Geometry& g, int pos, const TablesPtrs& t, cudaStream_t st);
+cudaError_t launch_logu_lut(const Geometry& g, const TablesPtrs& t, cudaStream_t st);
 cudaError_t launch_match_csr(const Geometry& g, int n, const TablesPtrs& t, const DecodePtrs& dp,
                              cudaStream_t st);
 cudaError_t launch_planes_build(const Geometry& g, int n_prefill, const TablesPtrs& t, cudaStream_t st);

@@ -31,7 +31,7 @@ def test_c_caller_sees_the_documented_codes_and_sizes(mp, tmp_path):
                     "-Wl,-rpath," + libdir, "-o", exe], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
     got = dict(line.split(" ", 1) for line in out.strip().splitlines())
-    assert int(got["abi"]) == 3
+    assert int(got["abi"]) == 4
     assert int(got["sizeof_config"]) == ctypes.sizeof(mp.mp_config)
     assert int(got["sizeof_tables_layout"]) == ctypes.sizeof(mp.mp_tables_layout)
     assert int(got["sizeof_decode_layout"]) == ctypes.sizeof(mp.mp_decode_layout)

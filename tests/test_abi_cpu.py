@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(mp):
     for n in names:
         assert getattr(lib, n) is not None
     assert set(mp.EXPORTED) <= set(names)
-    assert mp.mp_abi_version() == 3
+    assert mp.mp_abi_version() == 4
 
 
 def _cfg(mp, **kw):
@@ -76,13 +76,14 @@ def test_layouts_are_aligned_disjoint_and_sized(mp):
     c = _cfg(mp, layers=2, w_per_layer=True)
     t = mp.mp_tables_layout_get(c)
     names = ["header", "center", "beta", "ones", "negbeta_f32", "wt_f32", "wt_bf16", "center_parts", "codes", "csr_offsets",
-             "csr_ids"]
+             "csr_ids", "logu_lut"]
     offs = [getattr(t, n) for n in names]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and len(set(offs)) == len(offs)
     U, L, cap, d = 2 * 1 * 2, 75, 4096, 128
     assert t.csr_offsets - t.codes >= U * L * cap * 2
-    assert t.total_bytes - t.csr_ids >= U * L * cap * 2
+    assert t.logu_lut - t.csr_ids >= U * L * cap * 2
+    assert t.total_bytes - t.logu_lut >= (4096 + 1) * 4                # -log u on the cosine grid
     assert t.tc_cols == 768 and t.n_buckets == 256
     assert t.wt_bf16 - t.wt_f32 >= 2 * 768 * d * 4
     assert t.center_parts - t.wt_bf16 >= 2 * 3 * 768 * d * 2      # hi, mid, lo bf16 terms of W
