@@ -150,32 +150,56 @@ __device__ __forceinline__ uint32_t sign_word(const uint32_t (&r)[32]) {
   return ~__brev((w0 << 24) | (w1 << 16) | (w2 << 8) | w3);
 }
 
-// Codes of one part of a 256-column tile with K known at compile time: the column,
-// word and shift of every code are constants, so cutting a code is one or two shifts.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// sign bits of 16 accumulator columns in bits 0..15 (as sign_word)
+__device__ __forceinline__ uint32_t sign_word16(const uint32_t (&r)[16]) {
+  uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w0 = __funnelshift_l(r[i], w0, 1);
+    w1 = __funnelshift_l(r[8 + i], w1, 1);
+  }
+  return ~__brev((w0 << 24) | (w1 << 16)) & 0xffffu;
+}
+
+// Codes of one part of a 256-column tile with K known at compile time. The tile's used
+// 32-column chunks are split evenly over the kParts warps of a lane quarter; a part
+// cuts the codes of the tables that start in its chunks, and when its last table runs
+// into the next part's first chunk it also reads that chunk's first 16 columns. The
+// column, word and shift of every code are constants, so cutting a code is one or two
+// shifts.
 template <int KC, int PART>
 __device__ __forceinline__ void epi_tile_k(uint32_t tbase, uint16_t* codes, int64_t u, int L, int cap, int row,
                                            bool store, int n) {
   constexpr int TPT = 256 / KC;
-  constexpr int TP = (TPT + kParts - 1) / kParts;
-  constexpr int TL0 = (PART * TP < TPT) ? PART * TP : TPT;
-  constexpr int TL1 = (TL0 + TP < TPT) ? TL0 + TP : TPT;
+  constexpr int NCT = (TPT * KC + 31) / 32;  // chunks holding whole tables
+  constexpr int CH0 = PART * NCT / kParts, CH1 = (PART + 1) * NCT / kParts;  // this part's chunks
+  constexpr int TL0 = (CH0 * 32 + KC - 1) / KC;
+  constexpr int TL1c = (CH1 * 32 + KC - 1) / KC;
+  constexpr int TL1 = TL1c < TPT ? TL1c : TPT;  // tables starting in [CH0, CH1)
   if constexpr (TL0 < TL1) {
-    constexpr int C0 = TL0 * KC, C1 = TL1 * KC;
-    constexpr int CH0 = C0 / 32, CH1 = (C1 - 1) / 32, NCH = CH1 - CH0 + 1;
+    constexpr int NCH = CH1 - CH0;
+    constexpr bool NEXT = (TL1 - 1) * KC + KC > CH1 * 32;  // the last table reaches chunk CH1
+    static_assert(!NEXT || (TL1 - 1) * KC + KC <= CH1 * 32 + 16, "a code reaches at most 16 columns on");
     uint32_t words[NCH + 1];
-    // three 32-column loads in flight per wait
-#pragma unroll
-    for (int i = 0; i < NCH; i += 3) {
-      uint32_t r0[32], r1[32], r2[32];
-      tmem_ld32(tbase + uint32_t((CH0 + i) * 32), r0);
-      if (i + 1 < NCH) tmem_ld32(tbase + uint32_t((CH0 + i + 1) * 32), r1);
-      if (i + 2 < NCH) tmem_ld32(tbase + uint32_t((CH0 + i + 2) * 32), r2);
-      tmem_wait_ld();
-      words[i] = sign_word(r0);
-      if (i + 1 < NCH) words[i + 1] = sign_word(r1);
-      if (i + 2 < NCH) words[i + 2] = sign_word(r2);
-    }
-    words[NCH] = 0u;
+    // every load of the part in flight before one wait (at most three chunks and a half)
+    static_assert(NCH <= 3, "at most three chunks per part");
+    uint32_t r0[32], r1[32], r2[32], rx[16];
+    tmem_ld32(tbase + uint32_t(CH0 * 32), r0);
+    if constexpr (NCH > 1) tmem_ld32(tbase + uint32_t((CH0 + 1) * 32), r1);
+    if constexpr (NCH > 2) tmem_ld32(tbase + uint32_t((CH0 + 2) * 32), r2);
+    if constexpr (NEXT) tmem_ld16(tbase + uint32_t(CH1 * 32), rx);
+    tmem_wait_ld();
+    words[0] = sign_word(r0);
+    if constexpr (NCH > 1) words[1] = sign_word(r1);
+    if constexpr (NCH > 2) words[2] = sign_word(r2);
+    words[NCH] = NEXT ? sign_word16(rx) : 0u;
     constexpr uint32_t MASK = (1u << KC) - 1u;
 #pragma unroll
     for (int tl = TL0; tl < TL1; ++tl) {
