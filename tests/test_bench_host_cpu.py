@@ -64,3 +64,15 @@ def test_roofline_arithmetic_of_the_long_context_job():
     assert r["frac"] == k["attend"]["achieved"] / 6000.0
     assert abs(sum(v["share"] for v in k.values()) - 1.0) < 1e-12
     assert out["build_ms"] == 14.0 and out["us_per_decode_step"] == 1e3 * 15.0 / 64
+
+
+def test_end_to_end_groups_split_layers_then_sequences():
+    """The end-to-end run issues the job in groups whose slices of K/V, W, queries and
+    outputs are whole layers (or, with one layer, whole sequences)."""
+    import workloads as WL
+    assert bench.e2e_groups(WL.WORKLOADS[2]) == ("layers", 8)      # 32 layers: groups of 4
+    assert bench.e2e_groups(WL.WORKLOADS[5]) == ("layers", 4)      # 4 layers: one each
+    assert bench.e2e_groups(WL.WORKLOADS[3]) == ("batch", 8)       # one layer, 16 sequences
+    assert bench.e2e_groups(WL.WORKLOADS[4]) == ("batch", 4)       # one layer, 4 sequences
+    assert bench.e2e_groups(WL.WORKLOADS[1]) == (None, 1)          # one layer, one sequence
+    assert bench.e2e_groups(WL.WORKLOADS[2].replace(layers=6)) == ("layers", 2)
