@@ -480,7 +480,8 @@ def summarize(job, wl, prof, pk, list_entries, sampled_entries, bucket_entries):
     # whole-job roofline: bytes at HBM bandwidth + hashing flops at tensor peak
     t_roof = sum(v[1] / (hbm * 1e9) for k, v in work.items() if v[0] == "bytes" and k in prof)
     t_roof += sum(v[1] / (tc * 1e12) for k, v in work.items() if v[0] == "flops" and k in prof)
-    build_ms = sum(prof[k][1] for k in ("prepare_w", "center", "hash_keys_tc", "hash_keys_simt", "csr_build")
+    build_ms = sum(prof[k][1] for k in ("prepare_w", "logu_lut", "center", "hash_keys_tc", "hash_keys_simt",
+                                        "csr_build", "planes_build")
                    if k in prof)
     dec_ms = total - build_ms
     x = 0.5 ** wl.K

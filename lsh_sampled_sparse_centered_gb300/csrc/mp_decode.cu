@@ -309,7 +309,9 @@ __device__ __forceinline__ float inclusion_prob(float x, int L, int threshold) {
   }
   const float T = float(threshold);
   if (Lf * x < 0.5f * T) {
-    float term = expf(lgammaf(Lf + 1.f) - lgammaf(T + 1.f) - lgammaf(Lf - T + 1.f) + T * logf(x) + (Lf - T) * l1x);
+    float lc = 0.f;  // log C(L, T) as a sum of T logs (T <= 7)
+    for (int i = 1; i <= threshold; ++i) lc += logf((Lf - T + float(i)) / float(i));
+    float term = expf(lc + T * logf(x) + (Lf - T) * l1x);
     float sum = term;
     for (int j = threshold; j < L && j < threshold + 24; ++j) {
       term *= (Lf - float(j)) / float(j + 1) * r;
@@ -327,57 +329,6 @@ __device__ __forceinline__ float inclusion_prob(float x, int L, int threshold) {
   return 1.f - head;
 }
 
-// The same probability in double precision, for the -log u table.
-__device__ double inclusion_prob_d(double x, int L, int threshold) {
-  if (x >= 1.0) return 1.0;
-  if (x <= 0.0) return 0.0;
-  const double Lf = double(L);
-  if (threshold <= 1) return -expm1(Lf * log1p(-x));
-  if (L < threshold) return 0.0;
-  const double l1x = log1p(-x);
-  const double r = x / (1.0 - x);
-  const double T = double(threshold);
-  if (Lf * x < 0.5 * T) {
-    // tail sum_{j >= T} C(L, j) x^j (1 - x)^(L - j), term by term
-    double term = exp(lgamma(Lf + 1.0) - lgamma(T + 1.0) - lgamma(Lf - T + 1.0) + T * log(x) + (Lf - T) * l1x);
-    double sum = term;
-    for (int j = threshold; j < L && j < threshold + 64; ++j) {
-      term *= (Lf - double(j)) / double(j + 1) * r;
-      sum += term;
-      if (term < 1e-17 * sum) break;
-    }
-    return sum;
-  }
-  // 1 - sum_{j < T} C(L, j) x^j (1 - x)^(L - j)
-  double term = exp(Lf * l1x);
-  double head = term;
-  for (int j = 0; j < threshold - 1; ++j) {
-    term *= (Lf - double(j)) / double(j + 1) * r;
-    head += term;
-  }
-  return 1.0 - head;
-}
-
-// lut[i] = -log u at the cosine kLutLo + i (kLutHi - kLutLo) / kLutN: p = 1 - acos/pi,
-// x = p^K, u = P[Bin(L, x) >= threshold] (Eq. 10/11), u floored at 1e-30 as in the
-// attention's direct evaluation; the header records which (K, L, threshold) it holds.
-__global__ void k_logu_lut(float* __restrict__ lut, DevHeader* hdr, int K, int L, int threshold) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i <= kLutN) {
-    const double cs = double(kLutLo) + (double(kLutHi) - double(kLutLo)) * double(i) / double(kLutN);
-    const double p = 1.0 - acos(cs) / CUDART_PI;
-    double x = 1.0;
-    for (int k = 0; k < K; ++k) x *= p;
-    lut[i] = float(-log(fmax(inclusion_prob_d(x, L, threshold), 1e-30)));
-  }
-  if (i == 0) hdr->lut_key = lut_key_of(K, L, threshold);
-}
-
-cudaError_t launch_logu_lut(const Geometry& g, const TablesPtrs& t, cudaStream_t st) {
-  k_logu_lut<<<(kLutN + 1 + 127) / 128, 128, 0, st>>>(t.lut, t.hdr, g.K, g.L, g.threshold);
-  return cudaGetLastError();
-}
-
 // -log u evaluated directly (cosines outside the table, or no table for this config)
 __device__ __noinline__ float neg_log_u(float cs, int K, int L, int threshold) {
   const float p = 1.f - acosf(cs) * (1.f / CUDART_PI_F);
@@ -389,6 +340,20 @@ __device__ __noinline__ float neg_log_u(float cs, int K, int L, int threshold) {
     pb *= pb;
   }
   return -logf(fmaxf(inclusion_prob(x, L, threshold), 1e-30f));
+}
+
+// lut[i] = -log u at the cosine kLutLo + i (kLutHi - kLutLo) / kLutN, evaluated exactly as
+// the attention evaluates it outside the table; the header records which (K, L,
+// threshold) it holds.
+__global__ void k_logu_lut(float* __restrict__ lut, DevHeader* hdr, int K, int L, int threshold) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i <= kLutN) lut[i] = neg_log_u(kLutLo + float(i) * ((kLutHi - kLutLo) / float(kLutN)), K, L, threshold);
+  if (i == 0) hdr->lut_key = lut_key_of(K, L, threshold);
+}
+
+cudaError_t launch_logu_lut(const Geometry& g, const TablesPtrs& t, cudaStream_t st) {
+  k_logu_lut<<<(kLutN + 1 + 127) / 128, 128, 0, st>>>(t.lut, t.hdr, g.K, g.L, g.threshold);
+  return cudaGetLastError();
 }
 
 constexpr int kAttThreads = 128;

@@ -8,6 +8,11 @@ and the attention interpolates it; below -0.5 (u near zero) and above 0.99 (wher
 here: the stored table against the oracle's inclusion probability at every grid point,
 for several (K, L, T); and full parity on heads whose query is a key's centered vector
 (cosine 1 with that key: the direct branch) or its negative.
+
+The table holds the kernel's own fp32 evaluation (acosf, log1pf, expm1f and expf of
+arguments up to about L·|log(1 - x)|, a few units in the last place each), so it is
+compared with the fp64 oracle within 5e-5 absolute plus 1e-4 relative; a float32 model
+of the same steps stays within 1.3e-5 absolute for these configs.
 """
 import numpy as np
 import pytest
@@ -45,7 +50,7 @@ def test_table_matches_the_oracle(mp, K, L, T):
     cs = LUT_LO + (LUT_HI - LUT_LO) * np.arange(LUT_N + 1) / LUT_N
     p = 1.0 - np.arccos(cs) / np.pi
     want = -np.log(np.maximum(O.inclusion_probability(p, K, L, T), 1e-30))
-    np.testing.assert_allclose(got, want, rtol=2e-6, atol=2e-6)
+    np.testing.assert_allclose(got, want, rtol=1e-4, atol=5e-5)
 
 
 @pytest.mark.parametrize("sign", [1.0, -1.0])
