@@ -70,9 +70,9 @@ def test_end_to_end_groups_split_layers_then_sequences():
     """The end-to-end run issues the job in groups whose slices of K/V, W, queries and
     outputs are whole layers (or, with one layer, whole sequences)."""
     import workloads as WL
-    assert bench.e2e_groups(WL.WORKLOADS[2]) == ("layers", 8)      # 32 layers: groups of 4
+    assert bench.e2e_groups(WL.WORKLOADS[2]) == ("layers", 4)      # 32 layers: groups of 8
     assert bench.e2e_groups(WL.WORKLOADS[5]) == ("layers", 4)      # 4 layers: one each
-    assert bench.e2e_groups(WL.WORKLOADS[3]) == ("batch", 8)       # one layer, 16 sequences
+    assert bench.e2e_groups(WL.WORKLOADS[3]) == ("batch", 4)       # one layer, 16 sequences
     assert bench.e2e_groups(WL.WORKLOADS[4]) == ("batch", 4)       # one layer, 4 sequences
     assert bench.e2e_groups(WL.WORKLOADS[1]) == (None, 1)          # one layer, one sequence
     assert bench.e2e_groups(WL.WORKLOADS[2].replace(layers=6)) == ("layers", 2)
