@@ -357,6 +357,7 @@ cudaError_t launch_logu_lut(const Geometry& g, const TablesPtrs& t, cudaStream_t
 }
 
 constexpr int kAttThreads = 128;
+constexpr float kLazyMargin = 8.f;  // weights below e^8 between raises of the reference
 
 // ---------------------------------------------------------------------------------
 // attention with register gathers: each warp walks groups of list entries, every
@@ -493,6 +494,7 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
     qc += __shfl_xor_sync(0xffffffffu, qc, o);
   }
   const float qnorm = sqrtf(qq);  // norm of the hashed query
+  const float inv_qnorm = qnorm > 0.f ? 1.f / qnorm : 0.f;
   // this lane's row of the group after reduce_rows8
   const int ju = 4 * ((lane & (LPR / 2)) != 0) + 2 * ((lane & (LPR / 4)) != 0) + ((lane & (LPR / 8)) != 0);
   const float scale = rsqrtf(float(D));
@@ -565,8 +567,13 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
       if (!(rent & kExactFlag)) {
         // p = 1 - theta(q, k - c)/pi (CQ: theta(q - c, k - c)), u = P[Bin(L, p^K) >= threshold]
         // (Eq. 10/11)
-        const float kn = sqrtf(rkk);
-        float cs = (qnorm > 0.f && kn > 0.f) ? rnum / (qnorm * kn) : 0.f;
+        float cs;
+        if constexpr (CQ) {
+          const float kn = sqrtf(rkk);
+          cs = (qnorm > 0.f && kn > 0.f) ? rnum / (qnorm * kn) : 0.f;
+        } else {
+          cs = rkk > 0.f ? rnum * rsqrtf(rkk) * inv_qnorm : 0.f;
+        }
         cs = fminf(1.f, fmaxf(-1.f, cs));
         if (use_lut && cs >= kLutLo && cs <= kLutHi) {
           // -log u interpolated on the build-time table (staged in shared memory)
@@ -579,19 +586,31 @@ __global__ void __launch_bounds__(kAttThreads, sizeof(T) == 2 ? 4 : 3) k_attend_
         }
       }
     }
-    // group maximum (every row sits in LPR/8 lanes)
-    float mg = lg;
+    // The weights are exp(logit - m_run) for a reference m_run. With the query as it is,
+    // the reference is raised (to the running maximum, rescaling l and acc) only when a
+    // logit exceeds it by more than kLazyMargin: one vote per group instead of a maximum
+    // reduction, weights below e^kLazyMargin; the final normalisation and the merges
+    // (which carry each partial's reference) make the result independent of it. The
+    // centered-query instance keeps the exact running maximum (at its register limit the
+    // vote measured slower).
+    const bool raise = CQ ? true : __any_sync(0xffffffffu, lg > m_run + kLazyMargin);
+    float m_new = m_run;
+    if (raise) {
+      float mg = lg;  // group maximum (every row sits in LPR/8 lanes)
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
-    const float m_new = fmaxf(m_run, mg);
+      for (int o = 16; o >= 1; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+      m_new = fmaxf(m_run, mg);
+    }
     if (m_new == -CUDART_INF_F) continue;  // warp-uniform: nothing valid yet
-    const float alpha = (m_run == -CUDART_INF_F) ? 0.f : __expf(m_run - m_new);
-    // each lane's weights for its rows: the row lane's logit, shifted by the new maximum
+    const float alpha = raise ? ((m_run == -CUDART_INF_F) ? 0.f : __expf(m_run - m_new)) : 1.f;
+    // each lane's weights for its rows: the row lane's logit, shifted by the reference
     const float pw = (lg == -CUDART_INF_F) ? 0.f : __expf(lg - m_new);
     float ps = 0.f;
-    const uint64_t al2 = pk2(alpha, alpha);
+    if (raise) {
+      const uint64_t al2 = pk2(alpha, alpha);
 #pragma unroll
-    for (int i = 0; i < NP; ++i) acc2[i] = mul2(acc2[i], al2);
+      for (int i = 0; i < NP; ++i) acc2[i] = mul2(acc2[i], al2);
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const float p = __shfl_sync(0xffffffffu, pw, row_lane<LPR>(sub, u));
