@@ -68,3 +68,34 @@ def test_query_along_a_centered_key(mp, sign):
                 t["queries"][s, 0, 0, qh] = torch.from_numpy(sign * 4.0 * kc / np.linalg.norm(kc)).to(t["queries"].dtype)
     rep = check_workload(mp, wl, t, check_csr_tables=4)
     assert rep["heads"] == wl.q_heads * wl.steps
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_keys_at_every_cosine_with_the_query(mp, dtype):
+    """Keys placed at prescribed cosines a in [-0.95, 0.998] with the query around a
+    common point, with K = 1, L = 4, T = 1 so that even keys at a = -0.9 (p = 0.14) are
+    sampled often: the sampled set holds keys on both sides of the table's range and
+    inside it, and the output must match the oracle."""
+    wl = WL.Workload("cosines", layers=1, batch=1, kv_heads=1, q_heads=1, head_dim=64, n_prefill=2000, steps=1,
+                     append=False, K=1, L=4, dtype=dtype, seed=77, window=8)
+    t = WL.generate(wl)
+    rng = np.random.default_rng(77)
+    d, n = wl.head_dim, wl.capacity
+    q = rng.standard_normal(d)
+    qh = q / np.linalg.norm(q)
+    c0 = 3.0 * rng.standard_normal(d)
+    a = rng.uniform(-0.95, 0.998, n)
+    a[::50] = 0.996  # some keys above the table's range for sure
+    r = rng.standard_normal((n, d))
+    r -= np.outer(r @ qh, qh)
+    r /= np.linalg.norm(r, axis=1, keepdims=True)
+    keys = c0 + 5.0 * (a[:, None] * qh + np.sqrt(1 - a[:, None] ** 2) * r)
+    t["keys"][0, 0, 0] = torch.from_numpy(keys).to(t["keys"].dtype)
+    t["queries"][0, 0, 0, 0] = torch.from_numpy(2.0 * q).to(t["queries"].dtype)
+    k64 = t["keys"][0, 0, 0].double().numpy()
+    kc = k64 - O.center_of_keys(k64, wl.n_sink, wl.n_prefill)
+    qq = t["queries"][0, 0, 0, 0].double().numpy()
+    cos = kc @ qq / np.linalg.norm(kc, axis=1) / np.linalg.norm(qq)
+    assert (cos < LUT_LO).sum() > 200 and (cos > LUT_HI).sum() > 20  # both sides of the table occur
+    rep = check_workload(mp, wl, t, threshold=1, check_csr_tables=wl.L)
+    assert rep["heads"] == 1 and rep["sampled"] > 1000
