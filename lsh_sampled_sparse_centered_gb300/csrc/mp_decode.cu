@@ -375,7 +375,7 @@ __device__ __forceinline__ uint4 ld_na(const uint4* p) {
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-constexpr int kListChunk = 1024;
+constexpr int kListChunk = 2048;
 
 // a 16-byte slice of a row as packed fp32 pairs: 4 pairs of bf16, or 2 pairs of fp32
 __device__ __forceinline__ void pairs_of(const uint4& v, const __nv_bfloat16*, uint64_t (&f)[4]) {
